@@ -1,0 +1,259 @@
+"""Oracle: a plain CPU restatement of the Muon step and AdamW.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py`` may import this package.  The GPU
+library never imports it, links it or runs it, and nothing here reads any
+value the GPU library produced.
+
+The arithmetic lives in ``muon_oracle.c`` (plain loops, fp64 accumulation,
+explicit bf16 round-to-nearest-even).  This module compiles it with gcc on
+first use and wraps it with ctypes over numpy arrays.
+
+Sources are cited by page title and section:
+  [OPT] "LLM training series, part 2: optimizers" (mhpq.cn article)
+  [K2]  "Kimi K2 ... what is worth noting" (Zhihu answer by toothacher17)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "muon_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O3", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+          "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile muon_oracle.c into liboracle.so (gcc, no GPU involved)."""
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class MuonHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("momentum", ctypes.c_float), ("nesterov", ctypes.c_int),
+                ("ns_steps", ctypes.c_int), ("ns_a", ctypes.c_float),
+                ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float),
+                ("norm_eps", ctypes.c_float), ("rms_scale", ctypes.c_float)]
+
+
+class AdamwHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float),
+                ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
+                ("weight_decay", ctypes.c_float)]
+
+
+class PlanEntry(ctypes.Structure):
+    _fields_ = [("mat_idx", ctypes.c_int32), ("transposed", ctypes.c_int32),
+                ("group_id", ctypes.c_int32), ("slot", ctypes.c_int32),
+                ("chunk_id", ctypes.c_int32), ("pad_", ctypes.c_int32),
+                ("mp", ctypes.c_int64), ("np", ctypes.c_int64)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i64 = ctypes.c_int64
+            lib.oracle_bf16_from_f32.argtypes = [ctypes.c_float]
+            lib.oracle_bf16_from_f32.restype = ctypes.c_uint16
+            lib.oracle_bf16_encode.argtypes = [P, P, i64]
+            lib.oracle_bf16_encode.restype = None
+            lib.oracle_newton_schulz.argtypes = [P, i64, i64, ctypes.c_int,
+                                                 ctypes.c_float, ctypes.c_float,
+                                                 ctypes.c_float, ctypes.c_int]
+            lib.oracle_newton_schulz.restype = ctypes.c_int
+            lib.oracle_muon_step_matrix.argtypes = [P, P, P, i64, i64, P, P, P]
+            lib.oracle_muon_step_matrix.restype = ctypes.c_int
+            lib.oracle_adamw_step.argtypes = [P, P, P, P, i64, P, i64]
+            lib.oracle_adamw_step.restype = ctypes.c_int
+            lib.oracle_ws_bytes_per_matrix.argtypes = [i64, i64]
+            lib.oracle_ws_bytes_per_matrix.restype = i64
+            lib.oracle_plan.argtypes = [P, P, i64, i64, P]
+            lib.oracle_plan.restype = ctypes.c_int
+            lib.oracle_num_threads.argtypes = []
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return int(_load().oracle_num_threads())
+
+
+# --------------------------------------------------------------------------
+# bf16
+# --------------------------------------------------------------------------
+
+def bf16_bits(x) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round-to-nearest-even (uint16 array)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_bf16_encode(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def bf16_values(bits) -> np.ndarray:
+    """bf16 bit patterns -> the fp32 values they encode (exact widening)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_round(x) -> np.ndarray:
+    return bf16_values(bf16_bits(x))
+
+
+# --------------------------------------------------------------------------
+# Newton-Schulz
+# --------------------------------------------------------------------------
+
+QUINTIC = (3.4445, -4.7750, 2.0315)
+CUBIC = (1.5, -0.5, 0.0)  # [OPT] section 4.2: X <- (3X - X X^T X) / 2
+
+
+def newton_schulz(X, steps=5, coeffs=QUINTIC, emulate_bf16=True) -> np.ndarray:
+    """Run the NS iteration on a wide matrix X (rows <= cols).
+
+    emulate_bf16=True: X must hold bf16 values; A, B and each new X are
+    rounded to bf16 at the GPU's storage points.  emulate_bf16=False: pure
+    fp64, for the closed-form checks."""
+    X = np.array(X, dtype=np.float64, order="C", copy=True)
+    if X.ndim != 2 or X.shape[0] > X.shape[1]:
+        raise ValueError("newton_schulz expects a wide 2-D matrix")
+    a, b, c = (float(np.float32(v)) for v in coeffs)
+    rc = _load().oracle_newton_schulz(_ptr(X), X.shape[0], X.shape[1], int(steps),
+                                      a, b, c, 1 if emulate_bf16 else 0)
+    if rc:
+        raise RuntimeError(f"oracle_newton_schulz failed ({rc})")
+    return X
+
+
+# --------------------------------------------------------------------------
+# Muon step
+# --------------------------------------------------------------------------
+
+@dataclass
+class MuonConfig:
+    lr: float = 0.02
+    weight_decay: float = 0.1
+    momentum: float = 0.95
+    nesterov: bool = True
+    ns_steps: int = 5
+    ns_a: float = QUINTIC[0]
+    ns_b: float = QUINTIC[1]
+    ns_c: float = QUINTIC[2]
+    norm_eps: float = 1e-7
+    rms_scale: float = 0.2
+
+    def c_struct(self) -> MuonHparams:
+        return MuonHparams(self.lr, self.weight_decay, self.momentum,
+                           int(bool(self.nesterov)), int(self.ns_steps),
+                           self.ns_a, self.ns_b, self.ns_c, self.norm_eps,
+                           self.rms_scale)
+
+
+def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig()):
+    """One Muon step on one matrix.
+
+    W, M: fp32 (rows x cols).  G: fp32 values (a bf16 gradient is passed as
+    its exact fp32 widening).  Returns (W_new, M_new, X0, O) with X0 and O in
+    the wide orientation (min(rows,cols) x max(rows,cols)); inputs are not
+    modified."""
+    W = np.array(W, dtype=np.float32, order="C", copy=True)
+    M = np.array(M, dtype=np.float32, order="C", copy=True)
+    G = np.ascontiguousarray(G, dtype=np.float32)
+    if W.ndim != 2 or W.shape != G.shape or W.shape != M.shape:
+        raise ValueError("W, G, M must be equal-shaped 2-D arrays")
+    rows, cols = W.shape
+    mp, np_ = min(rows, cols), max(rows, cols)
+    X0 = np.empty((mp, np_), dtype=np.float32)
+    O = np.empty((mp, np_), dtype=np.float32)
+    h = hp.c_struct()
+    rc = _load().oracle_muon_step_matrix(_ptr(W), _ptr(G), _ptr(M), rows, cols,
+                                         ctypes.byref(h), _ptr(X0), _ptr(O))
+    if rc:
+        raise RuntimeError(f"oracle_muon_step_matrix failed ({rc})")
+    return W, M, X0, O
+
+
+# --------------------------------------------------------------------------
+# AdamW
+# --------------------------------------------------------------------------
+
+@dataclass
+class AdamwConfig:
+    lr: float = 3e-4
+    beta1: float = 0.9
+    beta2: float = 0.95
+    eps: float = 1e-8
+    weight_decay: float = 0.1
+
+    def c_struct(self) -> AdamwHparams:
+        return AdamwHparams(self.lr, self.beta1, self.beta2, self.eps,
+                            self.weight_decay)
+
+
+def adamw_step(p, g, m, v, hp: AdamwConfig = AdamwConfig(), t: int = 1):
+    """AdamW on flat fp32 buffers; returns new (p, m, v), inputs untouched."""
+    p = np.array(p, dtype=np.float32, order="C", copy=True).reshape(-1)
+    m = np.array(m, dtype=np.float32, order="C", copy=True).reshape(-1)
+    v = np.array(v, dtype=np.float32, order="C", copy=True).reshape(-1)
+    g = np.ascontiguousarray(g, dtype=np.float32).reshape(-1)
+    if not (p.size == g.size == m.size == v.size):
+        raise ValueError("p, g, m, v must have the same size")
+    h = hp.c_struct()
+    rc = _load().oracle_adamw_step(_ptr(p), _ptr(g), _ptr(m), _ptr(v), p.size,
+                                   ctypes.byref(h), int(t))
+    if rc:
+        raise RuntimeError(f"oracle_adamw_step failed ({rc})")
+    return p, m, v
+
+
+# --------------------------------------------------------------------------
+# Plan
+# --------------------------------------------------------------------------
+
+def ws_bytes_per_matrix(mp: int, np_: int) -> int:
+    return int(_load().oracle_ws_bytes_per_matrix(int(mp), int(np_)))
+
+
+def plan(shapes, ws_bytes: int) -> np.ndarray:
+    """Plan for a list of (rows, cols): structured array with fields
+    mat_idx, transposed, group_id, slot, chunk_id, mp, np (plan order)."""
+    shapes = list(shapes)
+    n = len(shapes)
+    rows = np.array([s[0] for s in shapes] or [0], dtype=np.int64)
+    cols = np.array([s[1] for s in shapes] or [0], dtype=np.int64)
+    out = (PlanEntry * max(n, 1))()
+    rc = _load().oracle_plan(_ptr(rows), _ptr(cols), n, int(ws_bytes),
+                             ctypes.cast(out, ctypes.c_void_p))
+    if rc:
+        raise ValueError(f"oracle_plan failed ({rc})")
+    dt = np.dtype([("mat_idx", np.int32), ("transposed", np.int32),
+                   ("group_id", np.int32), ("slot", np.int32),
+                   ("chunk_id", np.int32), ("pad_", np.int32),
+                   ("mp", np.int64), ("np", np.int64)])
+    arr = np.frombuffer(bytes(out), dtype=dt, count=max(n, 1)).copy()
+    return arr[:n]

@@ -1,0 +1,451 @@
+/*
+ * Oracle for the Muon optimizer step and the AdamW step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, deliberately
+ * unoptimised CPU restatement of what the GPU library computes.  Only the
+ * test suite, the smoke check and the benchmark's CPU-baseline leg may load
+ * it.  It shares no code, header, table or helper with the CUDA library, and
+ * it never reads anything the CUDA library produced.
+ *
+ * Sources, cited by page title and section:
+ *   [OPT]  "LLM training series, part 2: optimizers (SGD -> Adam -> AdamW ->
+ *          Muon)", mhpq.cn article.  Section numbers are the article's own.
+ *   [K2]   "Kimi K2 ... what is worth noting" (Zhihu answer by toothacher17).
+ *          Section numbers are the answer's own.
+ * Quantities the pages leave open (the quintic coefficients, the Nesterov
+ * form, the 0.2*sqrt(max(m,n)) update scale, the 1e-7 norm epsilon) are the
+ * values this library is specified to use; each reading is stated where used.
+ *
+ * Arithmetic conventions (the same ones the library documents):
+ *   - every scalar the method names (lr, mu, beta, ...) is an IEEE fp32 value;
+ *   - element-wise formulas are evaluated as separately rounded fp32
+ *     operations in the order written next to them (build with
+ *     -ffp-contract=off so no multiply-add is fused);
+ *   - every matrix product is accumulated in fp64 in ascending k order, then
+ *     rounded once to fp32; bf16 rounding is round-to-nearest-even of that
+ *     fp32 value (see oracle_bf16_from_f32).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* bf16 encoding                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 keeps the top 16 bits of an fp32 word (sign, 8 exponent bits, 7
+ * mantissa bits).  Round-to-nearest-even by definition: look at the 16
+ * dropped bits; above half -> round up, below half -> round down, exactly
+ * half -> round to the candidate whose last kept bit is 0.  NaN stays NaN
+ * (quiet bit forced), +-inf stays inf. */
+uint16_t oracle_bf16_from_f32(float x)
+{
+    uint32_t bits;
+    memcpy(&bits, &x, sizeof bits);
+    uint32_t exponent = (bits >> 23) & 0xffu;
+    uint32_t mantissa = bits & 0x7fffffu;
+    if (exponent == 0xffu) {
+        if (mantissa != 0)
+            return (uint16_t)((bits >> 16) | 0x40u);
+        return (uint16_t)(bits >> 16);
+    }
+    uint32_t kept = bits >> 16;
+    uint32_t dropped = bits & 0xffffu;
+    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))
+        kept += 1u; /* a carry into the exponent is the correct result */
+    return (uint16_t)kept;
+}
+
+float oracle_f32_from_bf16(uint16_t h)
+{
+    uint32_t bits = (uint32_t)h << 16;
+    float x;
+    memcpy(&x, &bits, sizeof x);
+    return x;
+}
+
+static float bf16_round(float x)
+{
+    return oracle_f32_from_bf16(oracle_bf16_from_f32(x));
+}
+
+void oracle_bf16_encode(const float* x, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_bf16_from_f32(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plain matrix product, fp64 accumulation                                   */
+/* ------------------------------------------------------------------------ */
+
+/* C[i][j] = sum_{k=0}^{K-1} A[i][k] * B[k][j], A is MxK, B is KxN, all
+ * row-major fp64.  Each C[i][j] is summed in ascending k with one fp64
+ * rounding per multiply and per add.  The loops run i, k, j only so the j
+ * loop reads B row-wise; that does not change any element's summation
+ * order.  Rows are independent and may run on several threads. */
+static void matmul_f64(const double* A, const double* B, double* C,
+                       int64_t M, int64_t K, int64_t N)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        double* c = C + i * N;
+        for (int64_t j = 0; j < N; ++j)
+            c[j] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double a = A[i * K + k];
+            const double* b = B + k * N;
+            for (int64_t j = 0; j < N; ++j)
+                c[j] += a * b[j];
+        }
+    }
+}
+
+static void transpose_f64(const double* X, double* XT, int64_t R, int64_t C)
+{
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t c = 0; c < C; ++c)
+            XT[c * R + r] = X[r * C + c];
+}
+
+/* ------------------------------------------------------------------------ */
+/* Newton-Schulz orthogonalisation                                           */
+/* ------------------------------------------------------------------------ */
+
+/* One odd matrix polynomial applied `steps` times to a wide X (rows <= cols):
+ *     A  = X X^T
+ *     B  = b A + c A A
+ *     X <- a X + B X
+ * [OPT] section 4.2 gives the iteration's purpose and the cubic member
+ * X <- (3X - X X^T X)/2, i.e. (a,b,c) = (1.5, -0.5, 0); the library's
+ * default is the quintic (a,b,c) = (3.4445, -4.7750, 2.0315), 5 steps.
+ *
+ * X is rows x cols, row-major, overwritten with the result.
+ * emulate_bf16 != 0: the GPU's storage points are reproduced: the input is
+ *   taken as given (already bf16 values), and A, B and the new X are each
+ *   rounded fp64 -> fp32 -> bf16 once per step; the two epilogues are fp32:
+ *       B = bf16( fl32(b*A) + fl32(c*float(A A)) )
+ *       X = bf16( fl32(a*X) + float(B X) )
+ * emulate_bf16 == 0: everything stays in fp64 (used to check the iteration
+ *   against its singular-value closed form). */
+int oracle_newton_schulz(double* X, int64_t rows, int64_t cols, int steps,
+                         float a, float b, float c, int emulate_bf16)
+{
+    if (rows <= 0 || cols <= 0 || steps < 0 || rows > cols)
+        return 1;
+    double* XT = (double*)malloc(sizeof(double) * rows * cols);
+    double* A = (double*)malloc(sizeof(double) * rows * rows);
+    double* AA = (double*)malloc(sizeof(double) * rows * rows);
+    double* Bm = (double*)malloc(sizeof(double) * rows * rows);
+    double* BX = (double*)malloc(sizeof(double) * rows * cols);
+    if (!XT || !A || !AA || !Bm || !BX) {
+        free(XT); free(A); free(AA); free(Bm); free(BX);
+        return 2;
+    }
+    for (int s = 0; s < steps; ++s) {
+        /* A = X X^T */
+        transpose_f64(X, XT, rows, cols);
+        matmul_f64(X, XT, A, rows, cols, rows);
+        if (emulate_bf16)
+            for (int64_t i = 0; i < rows * rows; ++i)
+                A[i] = bf16_round((float)A[i]);
+        /* B = b A + c A A */
+        matmul_f64(A, A, AA, rows, rows, rows);
+        for (int64_t i = 0; i < rows * rows; ++i) {
+            if (emulate_bf16) {
+                float t1 = b * (float)A[i];
+                float t2 = c * (float)AA[i];
+                Bm[i] = bf16_round(t1 + t2);
+            } else {
+                Bm[i] = (double)b * A[i] + (double)c * AA[i];
+            }
+        }
+        /* X = a X + B X */
+        matmul_f64(Bm, X, BX, rows, rows, cols);
+        for (int64_t i = 0; i < rows * cols; ++i) {
+            if (emulate_bf16) {
+                float t1 = a * (float)X[i];
+                X[i] = bf16_round(t1 + (float)BX[i]);
+            } else {
+                X[i] = (double)a * X[i] + BX[i];
+            }
+        }
+    }
+    free(XT); free(A); free(AA); free(Bm); free(BX);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Muon step for one matrix                                                  */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    float lr;           /* learning rate                                    */
+    float weight_decay; /* decoupled weight decay                           */
+    float momentum;     /* mu                                               */
+    int nesterov;       /* 1: Nesterov look-ahead, 0: plain EMA momentum    */
+    int ns_steps;       /* Newton-Schulz steps                              */
+    float ns_a, ns_b, ns_c;
+    float norm_eps;     /* added to the Frobenius norm                      */
+    float rms_scale;    /* update scale = rms_scale * sqrt(max(rows, cols)) */
+} oracle_muon_hparams;
+
+/* One Muon step on one rows x cols matrix, in place on W and M.
+ *   W   fp32 master weight (rows x cols, row-major), updated in place
+ *   G   gradient, fp32 values (a bf16 gradient is passed already widened:
+ *       the widening is exact)
+ *   M   fp32 momentum, updated in place
+ *   X0  optional out: the normalised bf16 NS input, as float values, in the
+ *       wide orientation (min x max)
+ *   O   optional out: the NS output, as float values, wide orientation
+ *
+ * Steps, in the order the method applies them:
+ *  1. momentum, an exponential moving average of the gradient
+ *     ([OPT] section 2.1):   M = fl(fl(mu*M) + fl((1-mu)*G))
+ *  2. Nesterov look-ahead, read as the same average taken one step further:
+ *        u = fl(fl((1-mu)*G) + fl(mu*M))        (nesterov = 1)
+ *        u = M                                   (nesterov = 0)
+ *  3. Frobenius normalisation: ||u||_F summed in fp64, element order;
+ *        s = float(1 / (sqrt(sum u^2) + eps))
+ *  4. X0 = bf16(fl(u*s)), transposed when rows > cols so that NS always
+ *     sees a wide matrix (the smaller Gram matrix X X^T)
+ *  5. NS as in oracle_newton_schulz (bf16 emulation on)
+ *  6. O = NS output transposed back to rows x cols
+ *  7. decoupled weight decay and the RMS-matched update ([OPT] section 3.1
+ *     for the decoupled form, [K2] section 3.1 for matching the update RMS
+ *     of AdamW):  both terms use the old W,
+ *        scale = float(rms_scale * sqrt(max(rows, cols)))     (fp64 -> fp32)
+ *        W = fl(W - fl(lr * fl(fl(wd*W) + fl(scale*O))))
+ * Returns 0 on success. */
+int oracle_muon_step_matrix(float* W, const float* G, float* M,
+                            int64_t rows, int64_t cols,
+                            const oracle_muon_hparams* hp,
+                            float* X0_out, float* O_out)
+{
+    if (rows <= 0 || cols <= 0 || !hp)
+        return 1;
+    const int64_t n = rows * cols;
+    const int transposed = rows > cols;
+    const int64_t mp = transposed ? cols : rows; /* wide rows */
+    const int64_t np = transposed ? rows : cols; /* wide cols */
+    const float mu = hp->momentum;
+    const float one_minus_mu = 1.0f - mu;
+
+    float* u = (float*)malloc(sizeof(float) * n);
+    double* X = (double*)malloc(sizeof(double) * n);
+    if (!u || !X) {
+        free(u); free(X);
+        return 2;
+    }
+    /* steps 1-2 */
+    for (int64_t i = 0; i < n; ++i) {
+        float gterm = one_minus_mu * G[i];
+        float mnew = mu * M[i] + gterm;
+        M[i] = mnew;
+        u[i] = hp->nesterov ? gterm + mu * mnew : mnew;
+    }
+    /* step 3 */
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        ss += (double)u[i] * (double)u[i];
+    const float s = (float)(1.0 / (sqrt(ss) + (double)hp->norm_eps));
+    /* step 4 */
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            double x0 = bf16_round(u[r * cols + c] * s);
+            if (transposed)
+                X[c * np + r] = x0;
+            else
+                X[r * np + c] = x0;
+        }
+    if (X0_out)
+        for (int64_t i = 0; i < n; ++i)
+            X0_out[i] = (float)X[i];
+    /* step 5 */
+    int rc = oracle_newton_schulz(X, mp, np, hp->ns_steps, hp->ns_a, hp->ns_b,
+                                  hp->ns_c, 1);
+    if (rc) {
+        free(u); free(X);
+        return 10 + rc;
+    }
+    if (O_out)
+        for (int64_t i = 0; i < n; ++i)
+            O_out[i] = (float)X[i];
+    /* steps 6-7 */
+    const float scale = (float)((double)hp->rms_scale * sqrt((double)np));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            float o = (float)(transposed ? X[c * np + r] : X[r * np + c]);
+            float w = W[r * cols + c];
+            float decay = hp->weight_decay * w;
+            float step = scale * o;
+            float delta = hp->lr * (decay + step);
+            W[r * cols + c] = w - delta;
+        }
+    free(u);
+    free(X);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* AdamW                                                                     */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+} oracle_adamw_hparams;
+
+/* AdamW on flat fp32 buffers, step t >= 1, in place on p, m, v.
+ * [OPT] section 2.3 gives Adam with bias correction and section 3.1 the
+ * decoupled weight decay:
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2
+ *   m_hat = m / (1-b1^t); v_hat = v / (1-b2^t)
+ *   p = p - lr * m_hat / (sqrt(v_hat) + eps) - lr * wd * p
+ * The bias-correction denominators are computed once in fp64 and rounded to
+ * fp32; everything else is separately rounded fp32 in this order:
+ *   m    = fl(fl(b1*m) + fl((1-b1)*g))
+ *   v    = fl(fl(b2*v) + fl((1-b2)*fl(g*g)))
+ *   upd  = fl( fl(m/bc1) / fl(sqrt(fl(v/bc2)) + eps) )
+ *   p    = fl(p - fl(lr * fl(upd + fl(wd*p))))
+ * with (1-b1), (1-b2) computed in fp32.  Returns 0 on success. */
+int oracle_adamw_step(float* p, const float* g, float* m, float* v, int64_t n,
+                      const oracle_adamw_hparams* hp, int64_t t)
+{
+    if (!hp || t < 1 || n < 0)
+        return 1;
+    const float bc1 = (float)(1.0 - pow((double)hp->beta1, (double)t));
+    const float bc2 = (float)(1.0 - pow((double)hp->beta2, (double)t));
+    const float one_minus_b1 = 1.0f - hp->beta1;
+    const float one_minus_b2 = 1.0f - hp->beta2;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float gi = g[i];
+        float mi = hp->beta1 * m[i] + one_minus_b1 * gi;
+        float g2 = gi * gi;
+        float vi = hp->beta2 * v[i] + one_minus_b2 * g2;
+        float m_hat = mi / bc1;
+        float v_hat = vi / bc2;
+        float den = sqrtf(v_hat) + hp->eps;
+        float upd = m_hat / den;
+        float decay = hp->weight_decay * p[i];
+        p[i] = p[i] - hp->lr * (upd + decay);
+        m[i] = mi;
+        v[i] = vi;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plan: grouping, orientation and chunking                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Per-matrix workspace bytes of the library, restated from its documented
+ * layout (not from its code): two wide X buffers (m' x ld(n') bf16), the A
+ * and B Gram buffers (m' x ld(m') bf16), each padded to 256 bytes, plus an
+ * 8 KiB per-matrix record; ld(x) = x rounded up to a multiple of 8. */
+static int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
+
+int64_t oracle_ws_bytes_per_matrix(int64_t mp, int64_t np)
+{
+    int64_t x = round_up(2 * mp * round_up(np, 8), 256);
+    int64_t g = round_up(2 * mp * round_up(mp, 8), 256);
+    return 2 * x + 2 * g + 8192;
+}
+
+typedef struct {
+    int32_t mat_idx, transposed, group_id, slot, chunk_id, pad_;
+    int64_t mp, np;
+} oracle_plan_entry;
+
+/* The plan orders matrices by (m', n') ascending with m' = min(rows, cols),
+ * n' = max(rows, cols), ties broken by the caller's index; transposed is
+ * rows > cols.  group_id numbers the distinct (m', n') pairs in that order.
+ * Matrices are packed into chunks in plan order: a new chunk starts when
+ * adding the next matrix's workspace would exceed ws_bytes.  slot counts the
+ * matrices of one group within one chunk.  The ordering is written out as an
+ * insertion sort so that stability is evident.  Returns 0 on success, 3 when
+ * a single matrix needs more than ws_bytes. */
+int oracle_plan(const int64_t* rows, const int64_t* cols, int64_t count,
+                int64_t ws_bytes, oracle_plan_entry* out)
+{
+    if (count < 0 || (count > 0 && (!rows || !cols || !out)))
+        return 1;
+    int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (count ? count : 1));
+    if (!order)
+        return 2;
+    for (int64_t i = 0; i < count; ++i) {
+        if (rows[i] <= 0 || cols[i] <= 0) {
+            free(order);
+            return 1;
+        }
+        order[i] = i;
+    }
+    for (int64_t i = 1; i < count; ++i) {
+        int64_t cur = order[i];
+        int64_t cm = rows[cur] < cols[cur] ? rows[cur] : cols[cur];
+        int64_t cn = rows[cur] < cols[cur] ? cols[cur] : rows[cur];
+        int64_t j = i - 1;
+        while (j >= 0) {
+            int64_t o = order[j];
+            int64_t om = rows[o] < cols[o] ? rows[o] : cols[o];
+            int64_t on = rows[o] < cols[o] ? cols[o] : rows[o];
+            if (om > cm || (om == cm && on > cn)) {
+                order[j + 1] = order[j];
+                --j;
+            } else {
+                break;
+            }
+        }
+        order[j + 1] = cur;
+    }
+    int32_t group = -1, chunk = 0, slot = 0;
+    int64_t prev_m = -1, prev_n = -1, used = 0;
+    for (int64_t k = 0; k < count; ++k) {
+        int64_t i = order[k];
+        int64_t mp = rows[i] < cols[i] ? rows[i] : cols[i];
+        int64_t np = rows[i] < cols[i] ? cols[i] : rows[i];
+        int64_t need = oracle_ws_bytes_per_matrix(mp, np);
+        if (need > ws_bytes) {
+            free(order);
+            return 3;
+        }
+        int new_group = (mp != prev_m || np != prev_n);
+        if (new_group)
+            ++group;
+        if (k > 0 && used + need > ws_bytes) {
+            ++chunk;
+            used = 0;
+            slot = 0;
+        } else if (new_group) {
+            slot = 0;
+        }
+        out[k].mat_idx = (int32_t)i;
+        out[k].transposed = rows[i] > cols[i];
+        out[k].group_id = group;
+        out[k].slot = slot;
+        out[k].chunk_id = chunk;
+        out[k].pad_ = 0;
+        out[k].mp = mp;
+        out[k].np = np;
+        ++slot;
+        used += need;
+        prev_m = mp;
+        prev_n = np;
+    }
+    free(order);
+    return 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
