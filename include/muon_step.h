@@ -1,0 +1,170 @@
+/*
+ * muon_step.h -- C ABI of the GB300 (sm_103a) Muon + AdamW optimizer step.
+ *
+ * Sources, cited by page title and section:
+ *   [OPT] "LLM training series, part 2: optimizers (SGD -> Adam -> AdamW ->
+ *         Muon)", mhpq.cn article.
+ *   [K2]  "Kimi K2 ... what is worth noting", Zhihu answer by toothacher17.
+ *
+ * The library is stateless.  Every tensor is owned by the caller; every call
+ * only enqueues work on the caller's CUDA stream and returns.  Pointers named
+ * "device" must be CUDA device (or managed) memory of the current device;
+ * pointers named "host" are ordinary host memory read before the call
+ * returns.  No exception crosses this boundary; errors are returned as a
+ * muon_status_t and describe host-side validation or launch failures, not
+ * asynchronous kernel faults.  `stream` is a cudaStream_t passed as void*
+ * (NULL = the legacy default stream).
+ *
+ * Layout: every matrix is row-major, contiguous, rows x cols = (out, in).
+ */
+#ifndef MUON_STEP_H
+#define MUON_STEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MUON_OK = 0,
+    MUON_ERR_INVALID_ARG = 1,          /* null pointer, bad size, bad hparam  */
+    MUON_ERR_UNSUPPORTED_DTYPE = 2,    /* g_dtype not MUON_F32 / MUON_BF16    */
+    MUON_ERR_MISALIGNED = 3,           /* pointer below its element alignment */
+    MUON_ERR_WORKSPACE_TOO_SMALL = 4,  /* a single matrix needs more          */
+    MUON_ERR_CUDA = 5,                 /* a CUDA runtime call failed          */
+    MUON_ERR_TIMEOUT = 6,              /* a kernel gave up on a bounded wait  */
+    MUON_ERR_NO_DEVICE = 7             /* no sm_103 device is current         */
+} muon_status_t;
+
+typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype_t;
+
+/* One hidden weight matrix under Muon.  All three buffers are device memory
+ * of rows*cols elements; W and M are fp32 and updated in place, G is read
+ * only.  W, M and fp32 G must be 4-byte aligned, bf16 G 2-byte aligned;
+ * 16-byte alignment enables the vectorised path.  Matrices of one call must
+ * not overlap one another. */
+typedef struct {
+    float* W;          /* device, fp32 master weight                         */
+    const void* G;     /* device, gradient, g_dtype                          */
+    float* M;          /* device, fp32 momentum buffer                       */
+    int64_t rows;      /* > 0                                                */
+    int64_t cols;      /* > 0                                                */
+    int32_t g_dtype;   /* muon_dtype_t                                       */
+    int32_t reserved;  /* must be 0                                          */
+} muon_matrix_t;
+
+/* Hyper-parameters of one Muon step, all applied as fp32 values.
+ * Defaults of the reference configuration: lr 0.02, weight_decay 0.1,
+ * momentum 0.95, nesterov 1, ns_steps 5, (ns_a, ns_b, ns_c) =
+ * (3.4445, -4.7750, 2.0315), norm_eps 1e-7, rms_scale 0.2. */
+typedef struct {
+    float lr;
+    float weight_decay;
+    float momentum;    /* mu in [0, 1]                                       */
+    int32_t nesterov;  /* 1: Nesterov look-ahead, 0: plain moving average   */
+    int32_t ns_steps;  /* Newton-Schulz steps, 0..100                        */
+    float ns_a, ns_b, ns_c;
+    float norm_eps;    /* added to the Frobenius norm, >= 0                  */
+    float rms_scale;   /* update = rms_scale * sqrt(max(rows, cols)) * O     */
+} muon_hparams_t;
+
+/* One row of the execution plan (see muon_plan). */
+typedef struct {
+    int32_t mat_idx;     /* index into the caller's matrix array           */
+    int32_t transposed;  /* 1 when rows > cols                             */
+    int32_t group_id;    /* index of the distinct (m', n') pair            */
+    int32_t slot;        /* position within (chunk, group)                 */
+    int32_t chunk_id;    /* workspace pass the matrix is processed in      */
+    int32_t reserved;
+    int64_t mp;          /* m' = min(rows, cols)                           */
+    int64_t np;          /* n' = max(rows, cols)                           */
+} muon_plan_entry_t;
+
+/* AdamW hyper-parameters, fp32. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+} adamw_hparams_t;
+
+/* Workspace bytes one matrix occupies while its chunk is processed:
+ *   2 * R(2 * m' * L(n')) + 2 * R(2 * m' * L(m')) + 8192
+ * R(x) = x rounded up to 256, L(x) = x rounded up to 8 (two bf16 X buffers
+ * of m' x n', the bf16 Gram buffers A = X X^T and B = bA + cA^2 of m' x m',
+ * and an 8 KiB record of pointers and norm partial sums).  0 on bad dims. */
+size_t muon_workspace_bytes_per_matrix(int64_t rows, int64_t cols);
+
+/* Workspace size for a call: the sum over all matrices when that fits in
+ * `budget_bytes` (one chunk), else the largest multiple-chunk requirement,
+ * max(budget_bytes, largest single matrix).  *out_bytes receives it. */
+muon_status_t muon_workspace_size(const muon_matrix_t* mats, int64_t count,
+                                  size_t budget_bytes, size_t* out_bytes);
+
+/* The execution plan for `count` matrices and a workspace of `ws_bytes`
+ * (host call; only rows/cols are read).  `out` (host, count entries)
+ * receives the matrices in execution order: sorted by (m', n') ascending,
+ * ties by caller index; chunks cut greedily so each chunk's summed
+ * muon_workspace_bytes_per_matrix <= ws_bytes.  Deterministic.
+ * [K2] section 2.2: fine-grained experts make many small matrices, which
+ * the grouped launches batch by shape. */
+muon_status_t muon_plan(const muon_matrix_t* mats, int64_t count,
+                        size_t ws_bytes, muon_plan_entry_t* out);
+
+/* One Muon step on `count` matrices (host array `mats`), enqueued on
+ * `stream`.  For every matrix, with m' = min(rows, cols), n' = max:
+ *   M  = mu M + (1-mu) G                       ([OPT] section 2.1)
+ *   u  = (1-mu) G + mu M    (nesterov = 1; u = M when 0)
+ *   X0 = bf16(u / (||u||_F + eps)), transposed to m' x n' when rows > cols
+ *   ns_steps times:  A = X X^T;  B = b A + c A A;  X = a X + B X
+ *                    (bf16 storage, fp32 accumulation; [OPT] section 4.2)
+ *   W  = W - lr (wd W + rms_scale sqrt(n') O),  O = final X in W's layout
+ *        (decoupled decay on the old W, [OPT] section 3.1; RMS matched to
+ *        AdamW's 0.2-0.4, [K2] section 3.1)
+ * `workspace` is device memory of `ws_bytes` (>= the largest single
+ * matrix's muon_workspace_bytes_per_matrix), 256-byte aligned; it must not
+ * be used by other work until the step has finished on `stream`.
+ * count == 0 is a no-op.  A kernel that gives up on a bounded wait records
+ * MUON_ERR_TIMEOUT in the workspace; read it with muon_query_status. */
+muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count,
+                                const muon_hparams_t* hp, void* workspace,
+                                size_t ws_bytes, void* stream);
+
+/* Newton-Schulz alone on a batch of `count` wide bf16 matrices (device,
+ * [count][mp][np] row-major, bf16 bit patterns, mp <= np), writing the
+ * result to X_out (same layout; may not alias X_in):
+ *   ns_steps times: A = X X^T; B = b A + c A A; X = a X + B X.
+ * workspace: device, >= count * muon_workspace_bytes_per_matrix(mp, np),
+ * 256-byte aligned.  X_in and X_out must be 16-byte aligned. */
+muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out,
+                                 int64_t count, int64_t mp, int64_t np,
+                                 int32_t ns_steps, float a, float b, float c,
+                                 void* workspace, size_t ws_bytes,
+                                 void* stream);
+
+/* AdamW on flat fp32 device buffers of n elements, in place on p, m, v
+ * ([OPT] sections 2.3 and 3.1), step >= 1:
+ *   bc1 = 1 - beta1^step, bc2 = 1 - beta2^step   (fp64 on the host -> fp32)
+ *   m = beta1 m + (1-beta1) g;  v = beta2 v + (1-beta2) g*g
+ *   p = p - lr ( (m/bc1) / (sqrt(v/bc2) + eps) + wd p )
+ * every operation a separately rounded fp32 op in that order (no fused
+ * multiply-add).  Buffers must be 4-byte aligned and must not overlap;
+ * 16-byte alignment enables the vectorised path.  n == 0 is a no-op. */
+muon_status_t adamw_step(float* p, const float* g, float* m, float* v,
+                         int64_t n, const adamw_hparams_t* hp, int64_t step,
+                         void* stream);
+
+/* Synchronises `stream`, reads and clears the status word a step left in
+ * `workspace`; returns MUON_OK or the recorded error (MUON_ERR_TIMEOUT). */
+muon_status_t muon_query_status(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* muon_status_string(muon_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t muon_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_STEP_H */

@@ -1,0 +1,452 @@
+// C ABI of the Muon / AdamW step: validation, the execution plan, the
+// workspace layout and the launch sequence.  Kernels live in
+// elementwise.cu and ns_gemm.cu.
+//
+// Workspace layout of one chunk of n matrices (n * 8192 record bytes plus
+// the X / Gram buffers of muon_workspace_bytes_per_matrix):
+//   [0, 256)                 header: int32 status word at offset 0
+//   [256, ...)               MatDesc[n]
+//   [.., +n*4096)            norm partial sums, 1024 floats per matrix
+//   [n*8192, ...)            per shape group of c matrices:
+//                              X0[c], X1[c]  (each R(2 m' L(n')) bytes)
+//                              A[c],  B[c]   (each R(2 m' L(m')) bytes)
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include "internal.h"
+
+using namespace muon;
+
+namespace {
+
+constexpr int32_t kVersion = 100;  // 0.1.0
+
+inline int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
+
+struct DeviceInfo {
+    int ok = -1;  // -1 unknown, 0 unsupported, 1 sm_103
+    int num_sms = 0;
+};
+
+muon_status_t device_info(int* num_sms) {
+    static std::mutex mu;
+    static DeviceInfo info[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_NO_DEVICE;
+    if (dev < 0 || dev >= 64) return MUON_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo& d = info[dev];
+    if (d.ok < 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MUON_ERR_CUDA;
+        d.ok = (major == 10 && minor == 3) ? 1 : 0;
+        d.num_sms = sms;
+    }
+    if (d.ok != 1) return MUON_ERR_NO_DEVICE;
+    *num_sms = d.num_sms;
+    return MUON_OK;
+}
+
+int64_t bytes_per_matrix(int64_t mp, int64_t np) {
+    const int64_t x = round_up(2 * mp * round_up(np, 8), 256);
+    const int64_t g = round_up(2 * mp * round_up(mp, 8), 256);
+    return 2 * x + 2 * g + static_cast<int64_t>(kRecordBytes);
+}
+
+bool finite(float x) { return isfinite(x) != 0; }
+
+muon_status_t check_hparams(const muon_hparams_t* hp) {
+    if (!hp) return MUON_ERR_INVALID_ARG;
+    if (!finite(hp->lr) || !finite(hp->weight_decay) || !finite(hp->momentum) || !finite(hp->ns_a) ||
+        !finite(hp->ns_b) || !finite(hp->ns_c) || !finite(hp->norm_eps) || !finite(hp->rms_scale))
+        return MUON_ERR_INVALID_ARG;
+    if (hp->momentum < 0.f || hp->momentum > 1.f || hp->norm_eps < 0.f) return MUON_ERR_INVALID_ARG;
+    if (hp->ns_steps < 0 || hp->ns_steps > 100) return MUON_ERR_INVALID_ARG;
+    if (hp->nesterov != 0 && hp->nesterov != 1) return MUON_ERR_INVALID_ARG;
+    return MUON_OK;
+}
+
+muon_status_t check_shapes(const muon_matrix_t* mats, int64_t count) {
+    if (count < 0) return MUON_ERR_INVALID_ARG;
+    if (count > 0 && !mats) return MUON_ERR_INVALID_ARG;
+    if (count > (int64_t(1) << 30)) return MUON_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < count; ++i) {
+        const muon_matrix_t& m = mats[i];
+        // m' and n' are used as int32 extents by the GEMM scheduler
+        if (m.rows <= 0 || m.cols <= 0 || m.rows > (int64_t(1) << 30) || m.cols > (int64_t(1) << 30))
+            return MUON_ERR_INVALID_ARG;
+        if (m.rows * m.cols > (int64_t(1) << 40)) return MUON_ERR_INVALID_ARG;
+    }
+    return MUON_OK;
+}
+
+muon_status_t check_pointers(const muon_matrix_t* mats, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) {
+        const muon_matrix_t& m = mats[i];
+        if (!m.W || !m.G || !m.M || m.reserved != 0) return MUON_ERR_INVALID_ARG;
+        if (m.g_dtype != MUON_F32 && m.g_dtype != MUON_BF16) return MUON_ERR_UNSUPPORTED_DTYPE;
+        const uintptr_t g_align = m.g_dtype == MUON_BF16 ? 2 : 4;
+        if ((reinterpret_cast<uintptr_t>(m.W) & 3u) || (reinterpret_cast<uintptr_t>(m.M) & 3u) ||
+            (reinterpret_cast<uintptr_t>(m.G) & (g_align - 1)))
+            return MUON_ERR_MISALIGNED;
+    }
+    return MUON_OK;
+}
+
+struct PlanRow {
+    int32_t idx, transposed, group, slot, chunk;
+    int64_t mp, np;
+};
+
+// Stable order by (m', n'); greedy chunks under ws_bytes.
+muon_status_t build_plan(const muon_matrix_t* mats, int64_t count, int64_t ws_bytes, std::vector<PlanRow>& out) {
+    std::vector<int32_t> order(static_cast<size_t>(count));
+    std::iota(order.begin(), order.end(), 0);
+    auto key = [&](int32_t i) {
+        const int64_t r = mats[i].rows, c = mats[i].cols;
+        return std::make_pair(std::min(r, c), std::max(r, c));
+    };
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return key(a) < key(b); });
+    out.clear();
+    out.reserve(order.size());
+    int32_t group = -1, chunk = 0, slot = 0;
+    int64_t used = 0, pm = -1, pn = -1;
+    for (size_t k = 0; k < order.size(); ++k) {
+        const int32_t i = order[k];
+        const auto mn = key(i);
+        const int64_t need = bytes_per_matrix(mn.first, mn.second);
+        if (need > ws_bytes) return MUON_ERR_WORKSPACE_TOO_SMALL;
+        const bool new_group = mn.first != pm || mn.second != pn;
+        if (new_group) ++group;
+        if (k > 0 && used + need > ws_bytes) {
+            ++chunk;
+            used = 0;
+            slot = 0;
+        } else if (new_group) {
+            slot = 0;
+        }
+        PlanRow row;
+        row.idx = i;
+        row.transposed = mats[i].rows > mats[i].cols ? 1 : 0;
+        row.group = group;
+        row.slot = slot++;
+        row.chunk = chunk;
+        row.mp = mn.first;
+        row.np = mn.second;
+        out.push_back(row);
+        used += need;
+        pm = mn.first;
+        pn = mn.second;
+    }
+    return MUON_OK;
+}
+
+muon_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA; }
+
+// Lays out one chunk's shape groups in the workspace.
+struct ChunkLayout {
+    std::vector<NsGroup> groups;
+    std::vector<int64_t> x0_of;  // per plan row in chunk: X0 address offset
+    std::vector<int64_t> x1_of;
+};
+
+void layout_groups(const std::vector<PlanRow>& plan, size_t b, size_t e, uint8_t* base, ChunkLayout& L) {
+    L.groups.clear();
+    L.x0_of.assign(e - b, 0);
+    L.x1_of.assign(e - b, 0);
+    uint8_t* cursor = base + (e - b) * kRecordBytes;
+    size_t k = b;
+    while (k < e) {
+        size_t j = k;
+        while (j < e && plan[j].mp == plan[k].mp && plan[j].np == plan[k].np) ++j;
+        const int64_t c = static_cast<int64_t>(j - k);
+        NsGroup g;
+        g.mp = plan[k].mp;
+        g.np = plan[k].np;
+        g.ldx = round_up(g.np, 8);
+        g.lda = round_up(g.mp, 8);
+        g.x_stride = round_up(2 * g.mp * g.ldx, 256);
+        g.g_stride = round_up(2 * g.mp * g.lda, 256);
+        g.count = c;
+        g.X[0] = reinterpret_cast<uint16_t*>(cursor);
+        g.X[1] = reinterpret_cast<uint16_t*>(cursor + c * g.x_stride);
+        g.A = reinterpret_cast<uint16_t*>(cursor + 2 * c * g.x_stride);
+        g.B = reinterpret_cast<uint16_t*>(cursor + 2 * c * g.x_stride + c * g.g_stride);
+        for (size_t q = k; q < j; ++q) {
+            L.x0_of[q - b] = reinterpret_cast<uint8_t*>(g.X[0]) - base + static_cast<int64_t>(q - k) * g.x_stride;
+            L.x1_of[q - b] = reinterpret_cast<uint8_t*>(g.X[1]) - base + static_cast<int64_t>(q - k) * g.x_stride;
+        }
+        cursor += 2 * c * g.x_stride + 2 * c * g.g_stride;
+        L.groups.push_back(g);
+        k = j;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t muon_version(void) { return kVersion; }
+
+const char* muon_status_string(muon_status_t s) {
+    switch (s) {
+        case MUON_OK: return "ok";
+        case MUON_ERR_INVALID_ARG: return "invalid argument";
+        case MUON_ERR_UNSUPPORTED_DTYPE: return "unsupported gradient dtype";
+        case MUON_ERR_MISALIGNED: return "misaligned pointer";
+        case MUON_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MUON_ERR_CUDA: return "CUDA runtime error";
+        case MUON_ERR_TIMEOUT: return "kernel timed out on a bounded wait";
+        case MUON_ERR_NO_DEVICE: return "no sm_103 device is current";
+    }
+    return "unknown status";
+}
+
+size_t muon_workspace_bytes_per_matrix(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return static_cast<size_t>(bytes_per_matrix(std::min(rows, cols), std::max(rows, cols)));
+}
+
+muon_status_t muon_workspace_size(const muon_matrix_t* mats, int64_t count, size_t budget_bytes,
+                                  size_t* out_bytes) {
+    if (!out_bytes) return MUON_ERR_INVALID_ARG;
+    muon_status_t s = check_shapes(mats, count);
+    if (s != MUON_OK) return s;
+    int64_t total = 0, largest = 0;
+    for (int64_t i = 0; i < count; ++i) {
+        const int64_t b = static_cast<int64_t>(muon_workspace_bytes_per_matrix(mats[i].rows, mats[i].cols));
+        total += b;
+        largest = std::max(largest, b);
+    }
+    const int64_t budget = static_cast<int64_t>(budget_bytes);
+    *out_bytes = static_cast<size_t>(total <= budget ? total : std::max(budget, largest));
+    return MUON_OK;
+}
+
+muon_status_t muon_plan(const muon_matrix_t* mats, int64_t count, size_t ws_bytes, muon_plan_entry_t* out) {
+    muon_status_t s = check_shapes(mats, count);
+    if (s != MUON_OK) return s;
+    if (count > 0 && !out) return MUON_ERR_INVALID_ARG;
+    std::vector<PlanRow> plan;
+    s = build_plan(mats, count, static_cast<int64_t>(ws_bytes), plan);
+    if (s != MUON_OK) return s;
+    for (size_t k = 0; k < plan.size(); ++k) {
+        out[k].mat_idx = plan[k].idx;
+        out[k].transposed = plan[k].transposed;
+        out[k].group_id = plan[k].group;
+        out[k].slot = plan[k].slot;
+        out[k].chunk_id = plan[k].chunk;
+        out[k].reserved = 0;
+        out[k].mp = plan[k].mp;
+        out[k].np = plan[k].np;
+    }
+    return MUON_OK;
+}
+
+muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const muon_hparams_t* hp,
+                                void* workspace, size_t ws_bytes, void* stream) {
+    muon_status_t s = check_hparams(hp);
+    if (s != MUON_OK) return s;
+    s = check_shapes(mats, count);
+    if (s != MUON_OK) return s;
+    if (count == 0) return MUON_OK;
+    s = check_pointers(mats, count);
+    if (s != MUON_OK) return s;
+    if (!workspace) return MUON_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_ERR_MISALIGNED;
+    int num_sms = 0;
+    s = device_info(&num_sms);
+    if (s != MUON_OK) return s;
+
+    std::vector<PlanRow> plan;
+    s = build_plan(mats, count, static_cast<int64_t>(ws_bytes), plan);
+    if (s != MUON_OK) return s;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws);
+    s = from_cuda(cudaMemsetAsync(status, 0, sizeof(int), st));
+    if (s != MUON_OK) return s;
+
+    const MomentumScalars ms{hp->momentum, 1.0f - hp->momentum, hp->nesterov};
+    const UpdateScalars us{hp->lr, hp->weight_decay};
+    ChunkLayout L;
+    std::vector<MatDesc> descs;
+    size_t b = 0;
+    while (b < plan.size()) {
+        size_t e = b;
+        while (e < plan.size() && plan[e].chunk == plan[b].chunk) ++e;
+        const int n = static_cast<int>(e - b);
+        layout_groups(plan, b, e, ws, L);
+        MatDesc* d_descs = reinterpret_cast<MatDesc*>(ws + kHeaderBytes);
+        float* d_partials = reinterpret_cast<float*>(
+            ws + kHeaderBytes + round_up(static_cast<int64_t>(n) * static_cast<int64_t>(sizeof(MatDesc)), 256));
+        descs.assign(n, MatDesc{});
+        int max_tiles = 1;
+        int64_t max_rows = 1, max_cols = 1;
+        for (int k = 0; k < n; ++k) {
+            const PlanRow& row = plan[b + k];
+            const muon_matrix_t& m = mats[row.idx];
+            MatDesc& d = descs[k];
+            d.W = m.W;
+            d.G = m.G;
+            d.M = m.M;
+            d.X0 = reinterpret_cast<uint16_t*>(ws + L.x0_of[k]);
+            d.O = reinterpret_cast<const uint16_t*>(ws + ((hp->ns_steps & 1) ? L.x1_of[k] : L.x0_of[k]));
+            d.partials = d_partials + static_cast<int64_t>(k) * kMaxNormTiles;
+            d.rows = m.rows;
+            d.cols = m.cols;
+            d.ldx = round_up(row.np, 8);
+            const int64_t nel = m.rows * m.cols;
+            int64_t tl = 8192;
+            int64_t nt = (nel + tl - 1) / tl;
+            if (nt > kMaxNormTiles) {
+                tl = round_up((nel + kMaxNormTiles - 1) / kMaxNormTiles, 8);
+                nt = (nel + tl - 1) / tl;
+            }
+            d.tile_len = tl;
+            d.ntiles = static_cast<int32_t>(nt);
+            d.g_bf16 = m.g_dtype == MUON_BF16 ? 1 : 0;
+            d.transposed = row.transposed;
+            d.vec = ((reinterpret_cast<uintptr_t>(m.W) | reinterpret_cast<uintptr_t>(m.G) |
+                      reinterpret_cast<uintptr_t>(m.M)) & 15u) == 0 ? 1 : 0;
+            d.scale = 0.f;
+            d.update_scale = static_cast<float>(static_cast<double>(hp->rms_scale) * sqrt(static_cast<double>(row.np)));
+            max_tiles = std::max(max_tiles, d.ntiles);
+            max_rows = std::max(max_rows, m.rows);
+            max_cols = std::max(max_cols, m.cols);
+        }
+        s = from_cuda(cudaMemcpyAsync(d_descs, descs.data(), sizeof(MatDesc) * n, cudaMemcpyHostToDevice, st));
+        if (s != MUON_OK) return s;
+        s = from_cuda(launch_momentum_norm(d_descs, n, max_tiles, ms, st));
+        if (s != MUON_OK) return s;
+        s = from_cuda(launch_norm_finalize(d_descs, n, hp->norm_eps, st));
+        if (s != MUON_OK) return s;
+        s = from_cuda(launch_normalize_cast(d_descs, n, max_rows, max_cols, ms, st));
+        if (s != MUON_OK) return s;
+        s = from_cuda(ns_run(L.groups.data(), static_cast<int>(L.groups.size()), hp->ns_steps, hp->ns_a, hp->ns_b,
+                             hp->ns_c, status, num_sms, st));
+        if (s != MUON_OK) return s;
+        s = from_cuda(launch_final_update(d_descs, n, max_rows, max_cols, us, st));
+        if (s != MUON_OK) return s;
+        b = e;
+    }
+    return MUON_OK;
+}
+
+muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t count, int64_t mp, int64_t np,
+                                 int32_t ns_steps, float a, float b, float c, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+    if (count < 0 || mp <= 0 || np <= 0 || mp > np || ns_steps < 0 || ns_steps > 100) return MUON_ERR_INVALID_ARG;
+    if (np > (int64_t(1) << 30)) return MUON_ERR_INVALID_ARG;
+    if (!finite(a) || !finite(b) || !finite(c)) return MUON_ERR_INVALID_ARG;
+    if (count == 0) return MUON_OK;
+    if (!X_in || !X_out || !workspace) return MUON_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(X_in) | reinterpret_cast<uintptr_t>(X_out)) & 1u) return MUON_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_ERR_MISALIGNED;
+    const int64_t per = bytes_per_matrix(mp, np);
+    if (per > static_cast<int64_t>(ws_bytes)) return MUON_ERR_WORKSPACE_TOO_SMALL;
+    int num_sms = 0;
+    muon_status_t s = device_info(&num_sms);
+    if (s != MUON_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws);
+    s = from_cuda(cudaMemsetAsync(status, 0, sizeof(int), st));
+    if (s != MUON_OK) return s;
+    const int64_t per_chunk = static_cast<int64_t>(ws_bytes) / per;
+    const size_t row_bytes = static_cast<size_t>(np) * 2;
+    for (int64_t first = 0; first < count; first += per_chunk) {
+        const int64_t cnt = std::min(per_chunk, count - first);
+        NsGroup g;
+        g.mp = mp;
+        g.np = np;
+        g.ldx = round_up(np, 8);
+        g.lda = round_up(mp, 8);
+        g.x_stride = round_up(2 * mp * g.ldx, 256);
+        g.g_stride = round_up(2 * mp * g.lda, 256);
+        g.count = cnt;
+        uint8_t* cursor = ws + cnt * static_cast<int64_t>(kRecordBytes);
+        g.X[0] = reinterpret_cast<uint16_t*>(cursor);
+        g.X[1] = reinterpret_cast<uint16_t*>(cursor + cnt * g.x_stride);
+        g.A = reinterpret_cast<uint16_t*>(cursor + 2 * cnt * g.x_stride);
+        g.B = reinterpret_cast<uint16_t*>(cursor + 2 * cnt * g.x_stride + cnt * g.g_stride);
+        for (int64_t k = 0; k < cnt; ++k) {
+            s = from_cuda(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(g.X[0]) + k * g.x_stride, g.ldx * 2,
+                                            X_in + (first + k) * mp * np, row_bytes, row_bytes, mp,
+                                            cudaMemcpyDeviceToDevice, st));
+            if (s != MUON_OK) return s;
+        }
+        s = from_cuda(ns_run(&g, 1, ns_steps, a, b, c, status, num_sms, st));
+        if (s != MUON_OK) return s;
+        const uint16_t* res = g.X[ns_steps & 1];
+        for (int64_t k = 0; k < cnt; ++k) {
+            s = from_cuda(cudaMemcpy2DAsync(X_out + (first + k) * mp * np, row_bytes,
+                                            reinterpret_cast<const uint8_t*>(res) + k * g.x_stride, g.ldx * 2,
+                                            row_bytes, mp, cudaMemcpyDeviceToDevice, st));
+            if (s != MUON_OK) return s;
+        }
+    }
+    return MUON_OK;
+}
+
+muon_status_t adamw_step(float* p, const float* g, float* m, float* v, int64_t n, const adamw_hparams_t* hp,
+                         int64_t step, void* stream) {
+    if (!hp || n < 0 || step < 1) return MUON_ERR_INVALID_ARG;
+    if (!finite(hp->lr) || !finite(hp->beta1) || !finite(hp->beta2) || !finite(hp->eps) ||
+        !finite(hp->weight_decay))
+        return MUON_ERR_INVALID_ARG;
+    if (hp->beta1 < 0.f || hp->beta1 >= 1.f || hp->beta2 < 0.f || hp->beta2 >= 1.f || hp->eps < 0.f)
+        return MUON_ERR_INVALID_ARG;
+    if (n == 0) return MUON_OK;
+    if (!p || !g || !m || !v) return MUON_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(m) |
+         reinterpret_cast<uintptr_t>(v)) & 3u)
+        return MUON_ERR_MISALIGNED;
+    // the four buffers must be pairwise disjoint
+    const uintptr_t lo[4] = {reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(g),
+                             reinterpret_cast<uintptr_t>(m), reinterpret_cast<uintptr_t>(v)};
+    const uintptr_t len = static_cast<uintptr_t>(n) * 4u;
+    for (int i = 0; i < 4; ++i)
+        for (int j = i + 1; j < 4; ++j)
+            if (lo[i] < lo[j] + len && lo[j] < lo[i] + len) return MUON_ERR_INVALID_ARG;
+    int num_sms = 0;
+    muon_status_t s = device_info(&num_sms);
+    if (s != MUON_OK) return s;
+    AdamwScalars sc;
+    sc.lr = hp->lr;
+    sc.beta1 = hp->beta1;
+    sc.beta2 = hp->beta2;
+    sc.one_minus_beta1 = 1.0f - hp->beta1;
+    sc.one_minus_beta2 = 1.0f - hp->beta2;
+    sc.bc1 = static_cast<float>(1.0 - pow(static_cast<double>(hp->beta1), static_cast<double>(step)));
+    sc.bc2 = static_cast<float>(1.0 - pow(static_cast<double>(hp->beta2), static_cast<double>(step)));
+    sc.eps = hp->eps;
+    sc.weight_decay = hp->weight_decay;
+    if (!(sc.bc1 > 0.f) || !(sc.bc2 > 0.f)) return MUON_ERR_INVALID_ARG;
+    return from_cuda(launch_adamw(p, g, m, v, n, sc, num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+muon_status_t muon_query_status(void* workspace, void* stream) {
+    if (!workspace) return MUON_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    if (cudaMemcpyAsync(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MUON_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MUON_ERR_CUDA;
+    if (host != 0) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MUON_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return MUON_ERR_CUDA;
+        return static_cast<muon_status_t>(host);
+    }
+    return MUON_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,417 @@
+// Element-wise stages of the Muon step and the AdamW step (HBM-bound).
+//
+//   momentum_norm   M = mu M + (1-mu) G;  u = (1-mu) G + mu M;  per-tile sum u^2
+//   norm_finalize   s = 1 / (sqrt(sum u^2) + eps) per matrix (fp64 sum)
+//   normalize_cast  X0 = bf16(u * s) in the wide orientation (smem transpose
+//                   for tall matrices)
+//   final_update    W = W - lr (wd W + scale O)
+//   adamw           AdamW on flat buffers
+//
+// Formulas follow "LLM training series, part 2: optimizers" (mhpq.cn):
+// momentum as an exponential moving average (section 2.1), Adam with bias
+// correction (section 2.3), decoupled weight decay (section 3.1).  Every
+// arithmetic step is an explicitly rounded fp32 intrinsic (__fmul_rn,
+// __fadd_rn, ...) so no multiply-add is contracted and the results are
+// reproducible bit for bit.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace muon {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 64;  // normalize / update tile edge
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ float load_g(const void* G, int g_bf16, int64_t i) {
+    return g_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(G)[i])
+                  : static_cast<const float*>(G)[i];
+}
+
+// Momentum update and Nesterov look-ahead for one element.
+__device__ __forceinline__ float momentum_elem(float g, float& m, const MomentumScalars& s) {
+    float gterm = __fmul_rn(s.one_minus_mu, g);
+    float mnew = __fadd_rn(__fmul_rn(s.mu, m), gterm);
+    m = mnew;
+    return s.nesterov ? __fadd_rn(gterm, __fmul_rn(s.mu, mnew)) : mnew;
+}
+
+// Look-ahead recomputed from the already updated momentum.
+__device__ __forceinline__ float lookahead_elem(float g, float mnew, const MomentumScalars& s) {
+    return s.nesterov ? __fadd_rn(__fmul_rn(s.one_minus_mu, g), __fmul_rn(s.mu, mnew)) : mnew;
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    if (warp == 0) {
+        t = lane < (kThreads / 32) ? red[lane] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    }
+    return t;
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1: momentum, look-ahead, per-tile sum of squares.
+// grid = (max tiles, matrices); each CTA handles one contiguous tile.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* __restrict__ descs,
+                                                                 MomentumScalars s) {
+    __shared__ float red[kThreads / 32];
+    const MatDesc& d = descs[blockIdx.y];
+    const int tile = blockIdx.x;
+    if (tile >= d.ntiles) return;
+    const int64_t n = d.rows * d.cols;
+    const int64_t start = static_cast<int64_t>(tile) * d.tile_len;
+    const int64_t end = min(n, start + d.tile_len);
+    float* __restrict__ M = d.M;
+    const void* G = d.G;
+    const int g_bf16 = d.g_bf16;
+    float acc = 0.f;
+    int64_t scalar_from = start;
+    if (d.vec) {
+        const int64_t nvec = (end - start) >> 3;
+        for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
+            const int64_t i = start + (v << 3);
+            float g[8];
+            if (g_bf16) {
+                uint4 raw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(G) + i));
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    g[2 * j] = __uint_as_float(w[j] << 16);
+                    g[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+                }
+            } else {
+                const float4* gp = reinterpret_cast<const float4*>(static_cast<const float*>(G) + i);
+                float4 a = __ldg(gp), b = __ldg(gp + 1);
+                g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+                g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+            }
+            float4* mp = reinterpret_cast<float4*>(M + i);
+            float4 m0 = mp[0], m1 = mp[1];
+            float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float u = momentum_elem(g[j], m[j], s);
+                acc = fmaf(u, u, acc);
+            }
+            mp[0] = make_float4(m[0], m[1], m[2], m[3]);
+            mp[1] = make_float4(m[4], m[5], m[6], m[7]);
+        }
+        scalar_from = start + (nvec << 3);
+    }
+    for (int64_t i = scalar_from + threadIdx.x; i < end; i += kThreads) {
+        float m = M[i];
+        float u = momentum_elem(load_g(G, g_bf16, i), m, s);
+        M[i] = m;
+        acc = fmaf(u, u, acc);
+    }
+    float total = block_sum(acc, red);
+    if (threadIdx.x == 0) d.partials[tile] = total;
+}
+
+// One warp per matrix: fp64 sum of the partials in a fixed order.
+__global__ void __launch_bounds__(kThreads) norm_finalize_kernel(MatDesc* __restrict__ descs,
+                                                                 int count, float eps) {
+    const int k = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (k >= count) return;
+    const MatDesc& d = descs[k];
+    double s = 0.0;
+    for (int i = lane; i < d.ntiles; i += 32) s += static_cast<double>(d.partials[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) descs[k].scale = static_cast<float>(1.0 / (sqrt(s) + static_cast<double>(eps)));
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: X0 = bf16(u * s), written in the wide orientation.
+// grid = (col tiles, row tiles, matrices) over the caller's orientation.
+// Thread (tx, ty) covers rows ty + 16 i (i < 4) and columns 4 tx .. 4 tx + 3.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const MatDesc* __restrict__ descs,
+                                                                  MomentumScalars s) {
+    __shared__ uint16_t tileT[kTile][kTile + 2];
+    const MatDesc& d = descs[blockIdx.z];
+    const int64_t rows = d.rows, cols = d.cols;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTile;
+    if (r0 >= rows || c0 >= cols) return;
+    const float scale = d.scale;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const bool full = d.vec && (cols % 4 == 0) && r0 + kTile <= rows && c0 + kTile <= cols;
+    const float* __restrict__ M = d.M;
+    const void* G = d.G;
+    const int g_bf16 = d.g_bf16;
+    uint16_t* __restrict__ X0 = d.X0;
+    const int64_t ldx = d.ldx;
+    const bool tr = d.transposed != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int rl = ty + 16 * i;
+        const int64_t r = r0 + rl;
+        const int64_t c = c0 + 4 * tx;
+        uint16_t b[4] = {0, 0, 0, 0};
+        if (full) {
+            const int64_t off = r * cols + c;
+            float4 m4 = *reinterpret_cast<const float4*>(M + off);
+            float g[4];
+            if (g_bf16) {
+                uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(G) + off);
+                g[0] = __uint_as_float(raw.x << 16); g[1] = __uint_as_float(raw.x & 0xffff0000u);
+                g[2] = __uint_as_float(raw.y << 16); g[3] = __uint_as_float(raw.y & 0xffff0000u);
+            } else {
+                float4 g4 = *reinterpret_cast<const float4*>(static_cast<const float*>(G) + off);
+                g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
+            }
+            const float m[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = f32_to_bf16(__fmul_rn(lookahead_elem(g[j], m[j], s), scale));
+            if (!tr) {
+                uint2 packed = make_uint2(b[0] | (static_cast<uint32_t>(b[1]) << 16),
+                                          b[2] | (static_cast<uint32_t>(b[3]) << 16));
+                *reinterpret_cast<uint2*>(X0 + r * ldx + c) = packed;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (r < rows && c + j < cols) {
+                    const int64_t off = r * cols + c + j;
+                    b[j] = f32_to_bf16(__fmul_rn(lookahead_elem(load_g(G, g_bf16, off), M[off], s), scale));
+                    if (!tr) X0[r * ldx + c + j] = b[j];
+                }
+            }
+        }
+        if (tr) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tileT[4 * tx + j][rl] = b[j];
+        }
+    }
+    if (!tr) return;
+    __syncthreads();
+    // transposed write: X0 row = original column, X0 column = original row
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int cl = ty + 16 * i;          // original column within tile
+        const int64_t xr = c0 + cl;          // X0 row
+        const int64_t xc = r0 + 4 * tx;      // X0 first column
+        if (xr >= cols) continue;
+        if (full) {
+            uint2 packed = make_uint2(tileT[cl][4 * tx] | (static_cast<uint32_t>(tileT[cl][4 * tx + 1]) << 16),
+                                      tileT[cl][4 * tx + 2] | (static_cast<uint32_t>(tileT[cl][4 * tx + 3]) << 16));
+            *reinterpret_cast<uint2*>(X0 + xr * ldx + xc) = packed;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (xc + j < rows) X0[xr * ldx + xc + j] = tileT[cl][4 * tx + j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Final update: W = W - lr (wd W + scale O), O read from the wide buffer.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float update_elem(float w, float o, float sc, const UpdateScalars& u) {
+    float decay = __fmul_rn(u.weight_decay, w);
+    float step = __fmul_rn(sc, o);
+    float delta = __fmul_rn(u.lr, __fadd_rn(decay, step));
+    return __fsub_rn(w, delta);
+}
+
+__global__ void __launch_bounds__(kThreads) final_update_kernel(const MatDesc* __restrict__ descs,
+                                                                UpdateScalars us) {
+    __shared__ uint16_t tileT[kTile][kTile + 2];
+    const MatDesc& d = descs[blockIdx.z];
+    const int64_t rows = d.rows, cols = d.cols;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTile;
+    if (r0 >= rows || c0 >= cols) return;
+    const float sc = d.update_scale;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const bool full = d.vec && (cols % 4 == 0) && r0 + kTile <= rows && c0 + kTile <= cols;
+    float* __restrict__ W = d.W;
+    const uint16_t* __restrict__ O = d.O;
+    const int64_t ldx = d.ldx;
+    const bool tr = d.transposed != 0;
+    if (tr) {
+        // stage O^T: O rows c0.., columns r0..
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int cl = ty + 16 * i;
+            const int64_t orow = c0 + cl;
+            const int64_t ocol = r0 + 4 * tx;
+            if (full) {
+                uint2 raw = *reinterpret_cast<const uint2*>(O + orow * ldx + ocol);
+                tileT[cl][4 * tx] = raw.x & 0xffffu; tileT[cl][4 * tx + 1] = raw.x >> 16;
+                tileT[cl][4 * tx + 2] = raw.y & 0xffffu; tileT[cl][4 * tx + 3] = raw.y >> 16;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    tileT[cl][4 * tx + j] = (orow < cols && ocol + j < rows) ? O[orow * ldx + ocol + j] : 0;
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int rl = ty + 16 * i;
+        const int64_t r = r0 + rl;
+        const int64_t c = c0 + 4 * tx;
+        if (full) {
+            float4* wp = reinterpret_cast<float4*>(W + r * cols + c);
+            float4 w4 = *wp;
+            uint16_t o[4];
+            if (tr) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) o[j] = tileT[4 * tx + j][rl];
+            } else {
+                uint2 raw = *reinterpret_cast<const uint2*>(O + r * ldx + c);
+                o[0] = raw.x & 0xffffu; o[1] = raw.x >> 16; o[2] = raw.y & 0xffffu; o[3] = raw.y >> 16;
+            }
+            w4.x = update_elem(w4.x, bf16_to_f32(o[0]), sc, us);
+            w4.y = update_elem(w4.y, bf16_to_f32(o[1]), sc, us);
+            w4.z = update_elem(w4.z, bf16_to_f32(o[2]), sc, us);
+            w4.w = update_elem(w4.w, bf16_to_f32(o[3]), sc, us);
+            *wp = w4;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (r < rows && c + j < cols) {
+                    uint16_t o = tr ? tileT[4 * tx + j][rl] : O[r * ldx + c + j];
+                    W[r * cols + c + j] = update_elem(W[r * cols + c + j], bf16_to_f32(o), sc, us);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// AdamW
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void adamw_elem(float& p, float g, float& m, float& v, const AdamwScalars& s) {
+    float mi = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.one_minus_beta1, g));
+    float g2 = __fmul_rn(g, g);
+    float vi = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(s.one_minus_beta2, g2));
+    float m_hat = __fdiv_rn(mi, s.bc1);
+    float v_hat = __fdiv_rn(vi, s.bc2);
+    float den = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
+    float upd = __fdiv_rn(m_hat, den);
+    float decay = __fmul_rn(s.weight_decay, p);
+    p = __fsub_rn(p, __fmul_rn(s.lr, __fadd_rn(upd, decay)));
+    m = mi;
+    v = vi;
+}
+
+__global__ void __launch_bounds__(kThreads) adamw_vec_kernel(float4* __restrict__ p, const float4* __restrict__ g,
+                                                             float4* __restrict__ m, float4* __restrict__ v,
+                                                             int64_t nvec, AdamwScalars s) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < nvec; i += stride) {
+        float4 pp = __ldcs(p + i), gg = __ldcs(g + i), mm = __ldcs(m + i), vv = __ldcs(v + i);
+        adamw_elem(pp.x, gg.x, mm.x, vv.x, s);
+        adamw_elem(pp.y, gg.y, mm.y, vv.y, s);
+        adamw_elem(pp.z, gg.z, mm.z, vv.z, s);
+        adamw_elem(pp.w, gg.w, mm.w, vv.w, s);
+        __stcs(p + i, pp);
+        __stcs(m + i, mm);
+        __stcs(v + i, vv);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) adamw_scalar_kernel(float* __restrict__ p, const float* __restrict__ g,
+                                                                float* __restrict__ m, float* __restrict__ v,
+                                                                int64_t begin, int64_t n, AdamwScalars s) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t i = begin + static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride) {
+        float pp = p[i], mm = m[i], vv = v[i];
+        adamw_elem(pp, g[i], mm, vv, s);
+        p[i] = pp;
+        m[i] = mm;
+        v[i] = vv;
+    }
+}
+
+inline unsigned grid_for(int64_t work, int64_t per_block, int64_t cap) {
+    int64_t b = (work + per_block - 1) / per_block;
+    if (b < 1) b = 1;
+    if (b > cap) b = cap;
+    return static_cast<unsigned>(b);
+}
+
+}  // namespace
+
+cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles, MomentumScalars s,
+                                 cudaStream_t st) {
+    for (int off = 0; off < count; off += 65535) {
+        int n = count - off < 65535 ? count - off : 65535;
+        momentum_norm_kernel<<<dim3(max_tiles, n), kThreads, 0, st>>>(descs + off, s);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, cudaStream_t st) {
+    const int per = kThreads / 32;
+    norm_finalize_kernel<<<(count + per - 1) / per, kThreads, 0, st>>>(descs, count, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_normalize_cast(const MatDesc* descs, int count, int64_t max_rows, int64_t max_cols,
+                                  MomentumScalars s, cudaStream_t st) {
+    const unsigned gx = static_cast<unsigned>((max_cols + kTile - 1) / kTile);
+    const unsigned gy = static_cast<unsigned>((max_rows + kTile - 1) / kTile);
+    if (gy > 65535u) return cudaErrorInvalidValue;
+    for (int off = 0; off < count; off += 65535) {
+        int n = count - off < 65535 ? count - off : 65535;
+        normalize_cast_kernel<<<dim3(gx, gy, n), kThreads, 0, st>>>(descs + off, s);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_final_update(const MatDesc* descs, int count, int64_t max_rows, int64_t max_cols,
+                                UpdateScalars s, cudaStream_t st) {
+    const unsigned gx = static_cast<unsigned>((max_cols + kTile - 1) / kTile);
+    const unsigned gy = static_cast<unsigned>((max_rows + kTile - 1) / kTile);
+    if (gy > 65535u) return cudaErrorInvalidValue;
+    for (int off = 0; off < count; off += 65535) {
+        int n = count - off < 65535 ? count - off : 65535;
+        final_update_kernel<<<dim3(gx, gy, n), kThreads, 0, st>>>(descs + off, s);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n, AdamwScalars s,
+                         int num_sms, cudaStream_t st) {
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const bool aligned = ((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(g) |
+                           reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+    int64_t done = 0;
+    if (aligned) {
+        const int64_t nvec = n / 4;
+        if (nvec > 0) {
+            adamw_vec_kernel<<<grid_for(nvec, kThreads, cap), kThreads, 0, st>>>(
+                reinterpret_cast<float4*>(p), reinterpret_cast<const float4*>(g),
+                reinterpret_cast<float4*>(m), reinterpret_cast<float4*>(v), nvec, s);
+        }
+        done = nvec * 4;
+    }
+    if (done < n) {
+        adamw_scalar_kernel<<<grid_for(n - done, kThreads, cap), kThreads, 0, st>>>(p, g, m, v, done, n, s);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace muon

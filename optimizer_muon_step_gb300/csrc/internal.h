@@ -1,0 +1,85 @@
+// Library-internal declarations shared by the CUDA translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "muon_step.h"
+
+namespace muon {
+
+// Per-matrix record the element-wise kernels read (device copy lives in the
+// workspace).  All buffers are row-major.  X buffers hold the wide
+// (m' x n') orientation with row stride `ldx`.
+struct MatDesc {
+    float* W;
+    const void* G;
+    float* M;
+    uint16_t* X0;        // NS input, bf16 bits
+    const uint16_t* O;   // NS output, bf16 bits (X0 or X1)
+    float* partials;     // per-tile sums of u^2 (kMaxNormTiles entries)
+    int64_t rows, cols;  // caller's orientation
+    int64_t ldx;         // row stride of X0 / O in elements
+    int64_t tile_len;    // elements per momentum tile (multiple of 8)
+    int32_t ntiles;      // momentum tiles
+    int32_t g_bf16;      // 1: G is bf16
+    int32_t transposed;  // 1: rows > cols, X holds the transpose
+    int32_t vec;         // 1: W, G, M are 16-byte aligned
+    float scale;         // 1 / (||u||_F + eps), written by the finalize kernel
+    float update_scale;  // rms_scale * sqrt(n')
+    int32_t pad_[2];
+};
+
+constexpr int kMaxNormTiles = 1024;
+constexpr size_t kRecordBytes = 8192;     // per matrix, see muon_step.h
+constexpr size_t kHeaderBytes = 256;      // status word lives at offset 0
+
+struct MomentumScalars {
+    float mu, one_minus_mu;
+    int32_t nesterov;
+};
+
+struct UpdateScalars {
+    float lr, weight_decay;
+};
+
+struct AdamwScalars {
+    float lr, beta1, beta2, one_minus_beta1, one_minus_beta2;
+    float bc1, bc2, eps, weight_decay;
+};
+
+// ---- element-wise kernels (elementwise.cu) --------------------------------
+cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles,
+                                 MomentumScalars s, cudaStream_t st);
+cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, cudaStream_t st);
+cudaError_t launch_normalize_cast(const MatDesc* descs, int count, int64_t max_rows,
+                                  int64_t max_cols, MomentumScalars s, cudaStream_t st);
+cudaError_t launch_final_update(const MatDesc* descs, int count, int64_t max_rows,
+                                int64_t max_cols, UpdateScalars s, cudaStream_t st);
+cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n,
+                         AdamwScalars s, int num_sms, cudaStream_t st);
+
+// ---- Newton-Schulz GEMMs (ns_gemm.cu) -------------------------------------
+// One shape group of wide bf16 matrices in the workspace: `count` matrices,
+// each X buffer [mp][ldx], each Gram buffer [mp][lda]; consecutive matrices
+// are `x_stride` / `g_stride` bytes apart.
+struct NsGroup {
+    uint16_t* X[2];
+    uint16_t* A;
+    uint16_t* B;
+    int64_t mp, np, ldx, lda;
+    int64_t x_stride, g_stride;  // bytes
+    int64_t count;
+};
+
+constexpr int kNsMaxGroups = 4;
+
+// Runs `steps` Newton-Schulz steps on every group; the result of each
+// group ends in X[steps % 2].  `status` is a device int the kernels set on a
+// bounded-wait timeout.  Returns a CUDA error or cudaSuccess; a tensor-map
+// encoding failure returns cudaErrorInvalidValue.
+cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, float a, float b,
+                   float c, int* status, int num_sms, cudaStream_t st);
+
+}  // namespace muon

@@ -1,0 +1,672 @@
+// Newton-Schulz orthogonalisation on Blackwell tensor cores (sm_103a).
+//
+// One step of the odd matrix polynomial on a batch of wide bf16 matrices X
+// (m' x n', m' <= n'), as three grouped GEMM launches:
+//
+//   SYRK    A = X X^T            upper-triangle tiles only, mirrored on store
+//   POLY    B = b A + c (A A)    upper-triangle tiles only, mirrored on store
+//   UPDATE  X' = a X + B X       all tiles
+//
+// The iteration is the one "LLM training series, part 2: optimizers"
+// (mhpq.cn, section 4.2) describes: it pushes the singular values of X
+// towards 1 without an SVD.  The cubic member there is (a, b, c) =
+// (1.5, -0.5, 0); the library's default is the quintic (3.4445, -4.7750,
+// 2.0315).  A and B are symmetric, so SYRK and POLY compute only tiles that
+// touch the upper triangle and store each element twice (A[r][c] and
+// A[c][r]); elements strictly below the diagonal come from their mirror.
+//
+// Kernel design (one persistent CTA per SM, 6 warps):
+//   warp 0       TMA producer: 128B-swizzled tiles of both operands into a
+//                4-stage shared-memory ring (mbarrier complete_tx)
+//   warp 1       TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
+//                M=128 N=256 K=16, fp32 accumulators in TMEM, two 256-column
+//                accumulator buffers so the epilogue of one tile overlaps the
+//                main loop of the next
+//   warps 2..5   epilogue: tcgen05.ld 32 lanes x 32 columns, fused
+//                polynomial / update arithmetic in fp32, bf16 stores
+// All operands are K-major except UPDATE's B operand (X read along its
+// rows, i.e. MN-major), which the descriptor's transpose bit handles, so no
+// matrix is ever transposed in memory.  Every wait is bounded: after
+// ~2 seconds a CTA records MUON_ERR_TIMEOUT, drains what it issued, frees
+// its TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace muon {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;  // two BN-column fp32 accumulators
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+enum Mode { MODE_SYRK = 0, MODE_POLY = 1, MODE_UPDATE = 2 };
+
+struct GroupParams {
+    CUtensorMap tm_a;      // A operand: rows of the left factor, K-major, box {64, 128}
+    CUtensorMap tm_b;      // B operand: K-major box {64, 256} or MN-major box {64, 64}
+    const uint16_t* E;     // epilogue addend (POLY: A, UPDATE: X)
+    uint16_t* D;           // output
+    int64_t ld;            // row stride of D and E, elements
+    int64_t bs;            // matrix stride of D and E, elements
+    int32_t M, N, K;
+    int32_t count;
+    int32_t tiles_n;
+    int32_t tiles_per_mat;
+    int32_t tile_begin;
+    int32_t pad_;
+};
+
+struct NsParams {
+    GroupParams g[kNsMaxGroups];
+    int32_t num_groups;
+    int32_t total_tiles;
+    float alpha;  // multiplies the addend E
+    float beta;   // multiplies the accumulator
+    int* status;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting
+// (another role timed out) or this wait itself ran past the limit, in which
+// case the abort flag and the global status word are set.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kTimeoutNs) {
+                *abort_flag = 1;
+                atomicCAS(status, 0, static_cast<int>(MUON_ERR_TIMEOUT));
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns; the wait is in the same asm block
+// so no use of the registers can be scheduled before the data has landed.
+__device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, sm_100 family layout:
+// start address, leading and stride byte offsets (all >> 4), fixed version
+// bits 46..48 = 0b001, swizzle mode 2 (128B) in bits 61..63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), B major-ness (bit 16), N >> 3 (bits 17-22),
+// M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t instr_desc(int m, int n, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+struct Tile {
+    int group, mat, ti, tj;
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(const NsParams& p, int t) {
+    Tile out;
+    int gi = 0;
+    while (gi + 1 < p.num_groups && t >= p.g[gi + 1].tile_begin) ++gi;
+    const GroupParams& g = p.g[gi];
+    int local = t - g.tile_begin;
+    out.group = gi;
+    out.mat = local / g.tiles_per_mat;
+    int r = local - out.mat * g.tiles_per_mat;
+    if (MODE == MODE_UPDATE) {
+        out.ti = r / g.tiles_n;
+        out.tj = r - out.ti * g.tiles_n;
+    } else {
+        // upper-triangle band: row tile ti keeps column tiles tj >= ti / 2
+        int ti = 0;
+        for (;;) {
+            const int cnt = g.tiles_n - (ti >> 1);
+            if (r < cnt) break;
+            r -= cnt;
+            ++ti;
+        }
+        out.ti = ti;
+        out.tj = (ti >> 1) + r;
+    }
+    return out;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_constant__ NsParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* tiles = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* full_bar = bars;
+    uint64_t* empty_bar = bars + STAGES;
+    uint64_t* tfull_bar = bars + 2 * STAGES;
+    uint64_t* tempty_bar = bars + 2 * STAGES + 2;
+    uint64_t* drain_bar = bars + 2 * STAGES + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull_bar[a]), 1);
+            mbar_init(smem_u32(&tempty_bar[a]), 4);
+        }
+        mbar_init(smem_u32(drain_bar), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        for (int gi = 0; gi < p.num_groups; ++gi) {
+            tma_prefetch_desc(&p.g[gi].tm_a);
+            tma_prefetch_desc(&p.g[gi].tm_b);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int last_parity[STAGES];
+        for (int s = 0; s < STAGES; ++s) last_parity[s] = -1;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+            const Tile tile = decode_tile<MODE>(p, t);
+            const GroupParams& g = p.g[tile.group];
+            const int nk = (g.K + BK - 1) / BK;
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&full_bar[stage]);
+                const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
+                const uint32_t sb = sa + A_BYTES;
+                mbar_expect_tx(fb, STAGE_BYTES);
+                tma_load_3d(sa, &g.tm_a, kb * BK, tile.ti * BM, tile.mat, fb);
+                if (MODE == MODE_UPDATE) {
+#pragma unroll
+                    for (int q = 0; q < BN / 64; ++q)
+                        tma_load_3d(sb + q * (64 * BK * 2), &g.tm_b, tile.tj * BN + 64 * q, kb * BK, tile.mat, fb);
+                } else {
+                    tma_load_3d(sb, &g.tm_b, kb * BK, tile.tj * BN, tile.mat, fb);
+                }
+                last_parity[stage] = static_cast<int>(phase);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        // drain: every issued copy must land before the CTA may exit
+        for (int s = 0; s < STAGES; ++s) {
+            if (last_parity[s] >= 0)
+                wait_bounded(smem_u32(&full_bar[s]), static_cast<uint32_t>(last_parity[s]), abort_flag, p.status);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t idesc = instr_desc(BM, BN, MODE == MODE_UPDATE);
+        int stage = 0;
+        uint32_t phase = 0;
+        int local = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++local) {
+            const Tile tile = decode_tile<MODE>(p, t);
+            const GroupParams& g = p.g[tile.group];
+            const int nk = (g.K + BK - 1) / BK;
+            const int acc = local & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+            if (!wait_bounded(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
+                const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    const uint64_t adesc = smem_desc(sa + k * 32, 16, 1024);
+                    const uint64_t bdesc = (MODE == MODE_UPDATE) ? smem_desc(sb + k * 16 * 128, 64 * BK * 2, 1024)
+                                                                 : smem_desc(sb + k * 32, 16, 1024);
+                    tc_mma(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&empty_bar[stage]));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            tc_commit(smem_u32(&tfull_bar[acc]));
+        }
+        // drain: all issued MMAs complete before TMEM is released
+        tc_commit(smem_u32(drain_bar));
+        wait_bounded(smem_u32(drain_bar), 0, abort_flag, p.status);
+    } else if (warp >= 2) {
+        // ---------------- epilogue ----------------
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        int local = 0;
+        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
+            const Tile tile = decode_tile<MODE>(p, t);
+            const GroupParams& g = p.g[tile.group];
+            const int acc = local & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
+            if (!wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status)) break;
+            tc_fence_after();
+            const int row_base = tile.ti * BM + quarter * 32;
+            const int row = row_base + lane;
+            const int64_t mat_off = static_cast<int64_t>(tile.mat) * g.bs;
+            uint16_t* __restrict__ D = g.D + mat_off;
+            const uint16_t* __restrict__ E = (MODE == MODE_SYRK) ? nullptr : g.E + mat_off;
+            const uint32_t t_addr = tmem_base + static_cast<uint32_t>(acc * BN) +
+                                    (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int col0 = tile.tj * BN + c * 32;
+                if (col0 >= g.N) break;                                        // warp-uniform
+                if (MODE != MODE_UPDATE && col0 + 31 < row_base) continue;   // below diagonal
+                __syncwarp();
+                float v[32];
+                tmem_load_32cols(t_addr + static_cast<uint32_t>(c * 32), v);
+                if (row >= g.M) continue;
+                const bool full_cols = col0 + 32 <= g.N;
+                if (MODE == MODE_UPDATE) {
+                    uint16_t* drow = D + static_cast<int64_t>(row) * g.ld + col0;
+                    const uint16_t* erow = E + static_cast<int64_t>(row) * g.ld + col0;
+                    if (full_cols) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 e = __ldg(reinterpret_cast<const uint4*>(erow) + q);
+                            const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const int j = q * 8 + h * 2;
+                                float lo = __fadd_rn(__fmul_rn(p.alpha, bf16_lo(ew[h])), v[j]);
+                                float hi = __fadd_rn(__fmul_rn(p.alpha, bf16_hi(ew[h])), v[j + 1]);
+                                o[h] = pack_bf16x2(lo, hi);
+                            }
+                            reinterpret_cast<uint4*>(drow)[q] = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (col0 + j < g.N) {
+                                float e = __uint_as_float(static_cast<uint32_t>(erow[j]) << 16);
+                                float val = __fadd_rn(__fmul_rn(p.alpha, e), v[j]);
+                                drow[j] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+                            }
+                        }
+                    }
+                } else {
+                    // symmetric output: store (row, col) for col >= row and the
+                    // mirror (col, row) for col > row
+                    uint16_t* drow = D + static_cast<int64_t>(row) * g.ld;
+                    const uint16_t* erow = (MODE == MODE_POLY) ? E + static_cast<int64_t>(row) * g.ld : nullptr;
+                    uint16_t out[32];
+                    if (MODE == MODE_POLY && full_cols) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 e = __ldg(reinterpret_cast<const uint4*>(erow + col0) + q);
+                            const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const int j = q * 8 + h * 2;
+                                float lo = __fadd_rn(__fmul_rn(p.alpha, bf16_lo(ew[h])), __fmul_rn(p.beta, v[j]));
+                                float hi = __fadd_rn(__fmul_rn(p.alpha, bf16_hi(ew[h])), __fmul_rn(p.beta, v[j + 1]));
+                                out[j] = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+                                out[j + 1] = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            float val = v[j];
+                            if (MODE == MODE_POLY) {
+                                const int col = col0 + j;
+                                float e = (col < g.N) ? __uint_as_float(static_cast<uint32_t>(erow[col]) << 16) : 0.f;
+                                val = __fadd_rn(__fmul_rn(p.alpha, e), __fmul_rn(p.beta, val));
+                            }
+                            out[j] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+                        }
+                    }
+                    if (full_cols && col0 >= row) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 w;
+                            w.x = out[q * 8 + 0] | (static_cast<uint32_t>(out[q * 8 + 1]) << 16);
+                            w.y = out[q * 8 + 2] | (static_cast<uint32_t>(out[q * 8 + 3]) << 16);
+                            w.z = out[q * 8 + 4] | (static_cast<uint32_t>(out[q * 8 + 5]) << 16);
+                            w.w = out[q * 8 + 6] | (static_cast<uint32_t>(out[q * 8 + 7]) << 16);
+                            reinterpret_cast<uint4*>(drow + col0)[q] = w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = col0 + j;
+                            if (col < g.N && col >= row) drow[col] = out[j];
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = col0 + j;
+                        if (col < g.N && col > row) D[static_cast<int64_t>(col) * g.ld + row] = out[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map over [count][rows][inner] with row stride ld elements
+// and matrix stride `mat_stride` bytes.
+bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t count, int64_t ld,
+              int64_t mat_stride, uint32_t box_inner, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(count)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(mat_stride)};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int triangle_tiles(int tiles_m, int tiles_n) {
+    int n = 0;
+    for (int ti = 0; ti < tiles_m; ++ti) n += tiles_n - (ti >> 1);
+    return n;
+}
+
+template <int MODE>
+cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, float b, float c, int* status,
+                         int num_sms, cudaStream_t st) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(ns_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    NsParams prm;
+    memset(&prm, 0, sizeof prm);
+    int tiles = 0;
+    for (int i = 0; i < ngroups; ++i) {
+        const NsGroup& G = groups[i];
+        GroupParams& g = prm.g[i];
+        const uint16_t* X = G.X[cur];
+        bool ok = true;
+        if (MODE == MODE_SYRK) {
+            ok &= make_map(&g.tm_a, X, G.np, G.mp, G.count, G.ldx, G.x_stride, BK, BM);
+            ok &= make_map(&g.tm_b, X, G.np, G.mp, G.count, G.ldx, G.x_stride, BK, BN);
+            g.E = nullptr;
+            g.D = G.A;
+            g.ld = G.lda;
+            g.bs = G.g_stride / 2;
+            g.M = static_cast<int32_t>(G.mp);
+            g.N = static_cast<int32_t>(G.mp);
+            g.K = static_cast<int32_t>(G.np);
+        } else if (MODE == MODE_POLY) {
+            ok &= make_map(&g.tm_a, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, BK, BM);
+            ok &= make_map(&g.tm_b, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, BK, BN);
+            g.E = G.A;
+            g.D = G.B;
+            g.ld = G.lda;
+            g.bs = G.g_stride / 2;
+            g.M = static_cast<int32_t>(G.mp);
+            g.N = static_cast<int32_t>(G.mp);
+            g.K = static_cast<int32_t>(G.mp);
+        } else {
+            ok &= make_map(&g.tm_a, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, BK, BM);
+            ok &= make_map(&g.tm_b, X, G.np, G.mp, G.count, G.ldx, G.x_stride, 64, BK);
+            g.E = X;
+            g.D = G.X[cur ^ 1];
+            g.ld = G.ldx;
+            g.bs = G.x_stride / 2;
+            g.M = static_cast<int32_t>(G.mp);
+            g.N = static_cast<int32_t>(G.np);
+            g.K = static_cast<int32_t>(G.mp);
+        }
+        if (!ok) return cudaErrorInvalidValue;
+        g.count = static_cast<int32_t>(G.count);
+        const int tiles_m = (g.M + BM - 1) / BM;
+        g.tiles_n = (g.N + BN - 1) / BN;
+        g.tiles_per_mat = (MODE == MODE_UPDATE) ? tiles_m * g.tiles_n : triangle_tiles(tiles_m, g.tiles_n);
+        g.tile_begin = tiles;
+        tiles += g.tiles_per_mat * g.count;
+    }
+    prm.num_groups = ngroups;
+    prm.total_tiles = tiles;
+    prm.status = status;
+    if (MODE == MODE_POLY) {
+        prm.alpha = b;
+        prm.beta = c;
+    } else if (MODE == MODE_UPDATE) {
+        prm.alpha = a;
+        prm.beta = 1.f;
+    } else {
+        prm.alpha = 0.f;
+        prm.beta = 1.f;
+    }
+    if (tiles == 0) return cudaSuccess;
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    ns_gemm_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, float a, float b, float c, int* status,
+                   int num_sms, cudaStream_t st) {
+    for (int s = 0; s < steps; ++s) {
+        const int cur = s & 1;
+        for (int off = 0; off < ngroups; off += kNsMaxGroups) {
+            const int n = ngroups - off < kNsMaxGroups ? ngroups - off : kNsMaxGroups;
+            cudaError_t e = launch_stage<MODE_SYRK>(groups + off, n, cur, a, b, c, status, num_sms, st);
+            if (e != cudaSuccess) return e;
+        }
+        for (int off = 0; off < ngroups; off += kNsMaxGroups) {
+            const int n = ngroups - off < kNsMaxGroups ? ngroups - off : kNsMaxGroups;
+            cudaError_t e = launch_stage<MODE_POLY>(groups + off, n, cur, a, b, c, status, num_sms, st);
+            if (e != cudaSuccess) return e;
+        }
+        for (int off = 0; off < ngroups; off += kNsMaxGroups) {
+            const int n = ngroups - off < kNsMaxGroups ? ngroups - off : kNsMaxGroups;
+            cudaError_t e = launch_stage<MODE_UPDATE>(groups + off, n, cur, a, b, c, status, num_sms, st);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
+}
+
+}  // namespace muon

@@ -80,6 +80,13 @@ def _load():
                                                  ctypes.c_float, ctypes.c_float,
                                                  ctypes.c_float, ctypes.c_int]
             lib.oracle_newton_schulz.restype = ctypes.c_int
+            lib.oracle_momentum.argtypes = [P, P, P, i64, ctypes.c_float, ctypes.c_int]
+            lib.oracle_momentum.restype = None
+            lib.oracle_normalize.argtypes = [P, i64, i64, ctypes.c_float, P]
+            lib.oracle_normalize.restype = ctypes.c_float
+            lib.oracle_final_update.argtypes = [P, P, i64, i64, ctypes.c_float, ctypes.c_float,
+                                                ctypes.c_float]
+            lib.oracle_final_update.restype = None
             lib.oracle_muon_step_matrix.argtypes = [P, P, P, i64, i64, P, P, P]
             lib.oracle_muon_step_matrix.restype = ctypes.c_int
             lib.oracle_adamw_step.argtypes = [P, P, P, P, i64, P, i64]
@@ -196,6 +203,38 @@ def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig()):
     if rc:
         raise RuntimeError(f"oracle_muon_step_matrix failed ({rc})")
     return W, M, X0, O
+
+
+def momentum(G, M, mu=0.95, nesterov=True):
+    """Steps 1-2 of the Muon step: returns (M_new, u), inputs untouched."""
+    G = np.ascontiguousarray(G, dtype=np.float32)
+    M = np.array(M, dtype=np.float32, order="C", copy=True)
+    if G.shape != M.shape:
+        raise ValueError("G and M must have the same shape")
+    u = np.empty_like(M)
+    _load().oracle_momentum(_ptr(G), _ptr(M), _ptr(u), M.size, float(mu), int(bool(nesterov)))
+    return M, u
+
+
+def normalize(u, eps=1e-7):
+    """Steps 3-4: returns (X0 wide as float values, s)."""
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    rows, cols = u.shape
+    X0 = np.empty((min(rows, cols), max(rows, cols)), dtype=np.float64)
+    s = _load().oracle_normalize(_ptr(u), rows, cols, float(eps), _ptr(X0))
+    return X0.astype(np.float32), float(s)
+
+
+def final_update(W, O, lr=0.02, weight_decay=0.1, rms_scale=0.2):
+    """Step 7 on W (rows x cols) with the wide NS output O; returns new W."""
+    W = np.array(W, dtype=np.float32, order="C", copy=True)
+    O = np.ascontiguousarray(O, dtype=np.float32)
+    rows, cols = W.shape
+    if O.shape != (min(rows, cols), max(rows, cols)):
+        raise ValueError("O must be the wide (min x max) NS output")
+    _load().oracle_final_update(_ptr(W), _ptr(O), rows, cols, float(lr), float(weight_decay),
+                                float(rms_scale))
+    return W
 
 
 # --------------------------------------------------------------------------

@@ -195,32 +195,82 @@ typedef struct {
     float rms_scale;    /* update scale = rms_scale * sqrt(max(rows, cols)) */
 } oracle_muon_hparams;
 
-/* One Muon step on one rows x cols matrix, in place on W and M.
- *   W   fp32 master weight (rows x cols, row-major), updated in place
- *   G   gradient, fp32 values (a bf16 gradient is passed already widened:
- *       the widening is exact)
- *   M   fp32 momentum, updated in place
- *   X0  optional out: the normalised bf16 NS input, as float values, in the
- *       wide orientation (min x max)
- *   O   optional out: the NS output, as float values, wide orientation
- *
- * Steps, in the order the method applies them:
+/* Steps 1-2 of the Muon step, element by element, in place on M:
  *  1. momentum, an exponential moving average of the gradient
  *     ([OPT] section 2.1):   M = fl(fl(mu*M) + fl((1-mu)*G))
  *  2. Nesterov look-ahead, read as the same average taken one step further:
  *        u = fl(fl((1-mu)*G) + fl(mu*M))        (nesterov = 1)
  *        u = M                                   (nesterov = 0)
- *  3. Frobenius normalisation: ||u||_F summed in fp64, element order;
- *        s = float(1 / (sqrt(sum u^2) + eps))
- *  4. X0 = bf16(fl(u*s)), transposed when rows > cols so that NS always
- *     sees a wide matrix (the smaller Gram matrix X X^T)
- *  5. NS as in oracle_newton_schulz (bf16 emulation on)
- *  6. O = NS output transposed back to rows x cols
- *  7. decoupled weight decay and the RMS-matched update ([OPT] section 3.1
- *     for the decoupled form, [K2] section 3.1 for matching the update RMS
- *     of AdamW):  both terms use the old W,
- *        scale = float(rms_scale * sqrt(max(rows, cols)))     (fp64 -> fp32)
- *        W = fl(W - fl(lr * fl(fl(wd*W) + fl(scale*O))))
+ * (1-mu) is computed in fp32.  u may be NULL. */
+void oracle_momentum(const float* G, float* M, float* u, int64_t n, float mu, int nesterov)
+{
+    const float one_minus_mu = 1.0f - mu;
+    for (int64_t i = 0; i < n; ++i) {
+        float gterm = one_minus_mu * G[i];
+        float mnew = mu * M[i] + gterm;
+        M[i] = mnew;
+        if (u)
+            u[i] = nesterov ? gterm + mu * mnew : mnew;
+    }
+}
+
+/* Steps 3-4: Frobenius normalisation and bf16 rounding.
+ *  3. ||u||_F summed in fp64 in element order; s = float(1/(sqrt(sum u^2)+eps))
+ *  4. X0 = bf16(fl(u*s)) written wide (min x max): transposed when rows > cols
+ *     so that NS works on the smaller Gram matrix X X^T.
+ * X0 is a (min x max) fp64 array of bf16 values.  Returns s. */
+float oracle_normalize(const float* u, int64_t rows, int64_t cols, float eps, double* X0)
+{
+    const int64_t n = rows * cols;
+    const int transposed = rows > cols;
+    const int64_t np = transposed ? rows : cols;
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        ss += (double)u[i] * (double)u[i];
+    const float s = (float)(1.0 / (sqrt(ss) + (double)eps));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            double x0 = bf16_round(u[r * cols + c] * s);
+            if (transposed)
+                X0[c * np + r] = x0;
+            else
+                X0[r * np + c] = x0;
+        }
+    return s;
+}
+
+/* Step 7: decoupled weight decay and the RMS-matched update ([OPT] section
+ * 3.1 for the decoupled form, [K2] section 3.1 for matching the update RMS
+ * of AdamW).  Both terms use the old W:
+ *    scale = float(rms_scale * sqrt(max(rows, cols)))     (fp64 -> fp32)
+ *    W = fl(W - fl(lr * fl(fl(wd*W) + fl(scale*O))))
+ * O is the NS output in the wide orientation (min x max, float values). */
+void oracle_final_update(float* W, const float* O, int64_t rows, int64_t cols,
+                         float lr, float weight_decay, float rms_scale)
+{
+    const int transposed = rows > cols;
+    const int64_t np = transposed ? rows : cols;
+    const float scale = (float)((double)rms_scale * sqrt((double)np));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            float o = transposed ? O[c * np + r] : O[r * np + c];
+            float w = W[r * cols + c];
+            float decay = weight_decay * w;
+            float step = scale * o;
+            float delta = lr * (decay + step);
+            W[r * cols + c] = w - delta;
+        }
+}
+
+/* One Muon step on one rows x cols matrix, in place on W and M:
+ * oracle_momentum, oracle_normalize, NS (oracle_newton_schulz with bf16
+ * emulation) on the wide matrix, oracle_final_update.
+ *   W   fp32 master weight (rows x cols, row-major), updated in place
+ *   G   gradient, fp32 values (a bf16 gradient is passed already widened:
+ *       the widening is exact)
+ *   M   fp32 momentum, updated in place
+ *   X0  optional out: the normalised bf16 NS input (wide, float values)
+ *   O   optional out: the NS output (wide, float values)
  * Returns 0 on success. */
 int oracle_muon_step_matrix(float* W, const float* G, float* M,
                             int64_t rows, int64_t cols,
@@ -230,65 +280,32 @@ int oracle_muon_step_matrix(float* W, const float* G, float* M,
     if (rows <= 0 || cols <= 0 || !hp)
         return 1;
     const int64_t n = rows * cols;
-    const int transposed = rows > cols;
-    const int64_t mp = transposed ? cols : rows; /* wide rows */
-    const int64_t np = transposed ? rows : cols; /* wide cols */
-    const float mu = hp->momentum;
-    const float one_minus_mu = 1.0f - mu;
-
+    const int64_t mp = rows > cols ? cols : rows;
+    const int64_t np = rows > cols ? rows : cols;
     float* u = (float*)malloc(sizeof(float) * n);
     double* X = (double*)malloc(sizeof(double) * n);
-    if (!u || !X) {
-        free(u); free(X);
+    float* O = (float*)malloc(sizeof(float) * n);
+    if (!u || !X || !O) {
+        free(u); free(X); free(O);
         return 2;
     }
-    /* steps 1-2 */
-    for (int64_t i = 0; i < n; ++i) {
-        float gterm = one_minus_mu * G[i];
-        float mnew = mu * M[i] + gterm;
-        M[i] = mnew;
-        u[i] = hp->nesterov ? gterm + mu * mnew : mnew;
-    }
-    /* step 3 */
-    double ss = 0.0;
-    for (int64_t i = 0; i < n; ++i)
-        ss += (double)u[i] * (double)u[i];
-    const float s = (float)(1.0 / (sqrt(ss) + (double)hp->norm_eps));
-    /* step 4 */
-    for (int64_t r = 0; r < rows; ++r)
-        for (int64_t c = 0; c < cols; ++c) {
-            double x0 = bf16_round(u[r * cols + c] * s);
-            if (transposed)
-                X[c * np + r] = x0;
-            else
-                X[r * np + c] = x0;
-        }
+    oracle_momentum(G, M, u, n, hp->momentum, hp->nesterov);
+    oracle_normalize(u, rows, cols, hp->norm_eps, X);
     if (X0_out)
         for (int64_t i = 0; i < n; ++i)
             X0_out[i] = (float)X[i];
-    /* step 5 */
     int rc = oracle_newton_schulz(X, mp, np, hp->ns_steps, hp->ns_a, hp->ns_b,
                                   hp->ns_c, 1);
     if (rc) {
-        free(u); free(X);
+        free(u); free(X); free(O);
         return 10 + rc;
     }
+    for (int64_t i = 0; i < n; ++i)
+        O[i] = (float)X[i];
     if (O_out)
-        for (int64_t i = 0; i < n; ++i)
-            O_out[i] = (float)X[i];
-    /* steps 6-7 */
-    const float scale = (float)((double)hp->rms_scale * sqrt((double)np));
-    for (int64_t r = 0; r < rows; ++r)
-        for (int64_t c = 0; c < cols; ++c) {
-            float o = (float)(transposed ? X[c * np + r] : X[r * np + c]);
-            float w = W[r * cols + c];
-            float decay = hp->weight_decay * w;
-            float step = scale * o;
-            float delta = hp->lr * (decay + step);
-            W[r * cols + c] = w - delta;
-        }
-    free(u);
-    free(X);
+        memcpy(O_out, O, sizeof(float) * n);
+    oracle_final_update(W, O, rows, cols, hp->lr, hp->weight_decay, hp->rms_scale);
+    free(u); free(X); free(O);
     return 0;
 }
 

@@ -1,0 +1,172 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header
+declares, validates its arguments, and its plan equals the oracle's bit for
+bit.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import optimizer_muon_step_gb300 as m
+import workloads
+from conftest import ROOT, cuda_available
+
+
+@pytest.fixture(scope="module")
+def built():
+    from optimizer_muon_step_gb300 import build
+    build.build()
+    return m.load_library()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "muon_step.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_symbols_exported(built):
+    names = header_functions()
+    assert set(names) == set(m.EXPORTS)
+    for name in names:
+        assert hasattr(built, name), name
+
+
+def test_version_and_status_strings(built):
+    assert m.version() >= 100
+    assert built.muon_status_string(0) == b"ok"
+    assert b"workspace" in built.muon_status_string(4)
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (7, 13), (13, 7), (2048, 2048), (5632, 2048), (1408, 2048),
+                                   (18432, 7168)])
+def test_workspace_bytes_match_oracle(built, shape):
+    r, c = shape
+    assert m.muon_workspace_bytes_per_matrix(r, c) == oracle.ws_bytes_per_matrix(min(r, c), max(r, c))
+
+
+def _plan_equal(shapes, ws):
+    got = m.muon_plan(shapes, ws)
+    ref = oracle.plan(shapes, ws)
+    for f in ("mat_idx", "transposed", "group_id", "slot", "chunk_id", "mp", "np"):
+        assert np.array_equal(got[f], ref[f]), f
+
+
+def test_plan_bit_exact_random(built):
+    rng = np.random.default_rng(5)
+    dims = [1, 7, 8, 64, 1408, 2048, 5632]
+    for _ in range(100):
+        n = int(rng.integers(0, 50))
+        shapes = [(int(rng.choice(dims)), int(rng.choice(dims))) for _ in range(n)]
+        need = max([oracle.ws_bytes_per_matrix(min(s), max(s)) for s in shapes] or [1])
+        _plan_equal(shapes, int(need * rng.uniform(1, 8)))
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+@pytest.mark.parametrize("budget_gb", [0.25, 4, 16, 1000])
+def test_plan_bit_exact_workloads(built, name, budget_gb):
+    shapes = [(s.rows, s.cols) for s in workloads.get(name).matrices]
+    largest = max(oracle.ws_bytes_per_matrix(min(s), max(s)) for s in shapes)
+    ws = max(int(budget_gb * 2 ** 30), largest)
+    _plan_equal(shapes, ws)
+
+
+def test_workspace_size_rule(built):
+    shapes = [(2048, 2048)] * 3 + [(7, 13)]
+    per = [oracle.ws_bytes_per_matrix(min(s), max(s)) for s in shapes]
+    assert m.muon_workspace_size(shapes, 1 << 40) == sum(per)
+    assert m.muon_workspace_size(shapes, 1) == max(per)
+    assert m.muon_workspace_size(shapes, max(per) + 10) == max(per) + 10
+
+
+def test_plan_rejects_small_workspace(built):
+    with pytest.raises(m.MuonError) as e:
+        m.muon_plan([(2048, 2048)], 4096)
+    assert e.value.status == 4
+
+
+def _hp():
+    return m.MuonHparams()._c()
+
+
+def test_step_argument_validation(built):
+    lib = built
+    arr = (m.MuonMatrix * 1)()
+    arr[0].W = arr[0].G = arr[0].M = 1024
+    arr[0].rows, arr[0].cols = 4, 4
+    ws = ctypes.c_void_p(4096)
+    # count 0 is a no-op, even without a device
+    assert lib.muon_step_batched(None, 0, ctypes.byref(_hp()), None, 0, None) == 0
+    # null hparams
+    assert lib.muon_step_batched(arr, 1, None, ws, 1 << 20, None) == 1
+    bad = _hp()
+    bad.momentum = 1.5
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(bad), ws, 1 << 20, None) == 1
+    bad = _hp()
+    bad.lr = float("nan")
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(bad), ws, 1 << 20, None) == 1
+    bad = _hp()
+    bad.ns_steps = -1
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(bad), ws, 1 << 20, None) == 1
+    # bad dims, dtype, alignment, workspace
+    arr[0].rows = 0
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(_hp()), ws, 1 << 20, None) == 1
+    arr[0].rows = 4
+    arr[0].g_dtype = 7
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(_hp()), ws, 1 << 20, None) == 2
+    arr[0].g_dtype = 0
+    arr[0].W = 1026
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(_hp()), ws, 1 << 20, None) == 3
+    arr[0].W = 1024
+    arr[0].reserved = 1
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(_hp()), ws, 1 << 20, None) == 1
+    arr[0].reserved = 0
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(_hp()), None, 1 << 20, None) == 1
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(_hp()), ctypes.c_void_p(4100), 1 << 20, None) == 3
+
+
+@pytest.mark.skipif(cuda_available(), reason="checks the no-device path")
+def test_step_without_device_reports_no_device(built):
+    arr = (m.MuonMatrix * 1)()
+    arr[0].W = arr[0].G = arr[0].M = 1024
+    arr[0].rows, arr[0].cols = 4, 4
+    st = built.muon_step_batched(arr, 1, ctypes.byref(_hp()), ctypes.c_void_p(4096), 1 << 20, None)
+    assert st == 7
+    h = m.AdamwHparams()._c()
+    assert built.adamw_step(ctypes.c_void_p(1024), ctypes.c_void_p(2048), ctypes.c_void_p(4096),
+                            ctypes.c_void_p(8192), 4, ctypes.byref(h), 1, None) == 7
+
+
+def test_adamw_argument_validation(built):
+    lib = built
+    h = m.AdamwHparams()._c()
+    P = ctypes.c_void_p
+    assert lib.adamw_step(None, None, None, None, 0, ctypes.byref(h), 1, None) == 0
+    assert lib.adamw_step(P(1024), P(2048), P(4096), P(8192), 4, ctypes.byref(h), 0, None) == 1
+    assert lib.adamw_step(None, P(2048), P(4096), P(8192), 4, ctypes.byref(h), 1, None) == 1
+    assert lib.adamw_step(P(1026), P(2048), P(4096), P(8192), 4, ctypes.byref(h), 1, None) == 3
+    # overlapping buffers
+    assert lib.adamw_step(P(1024), P(1028), P(4096), P(8192), 4, ctypes.byref(h), 1, None) == 1
+    bad = m.AdamwHparams(beta1=1.0)._c()
+    assert lib.adamw_step(P(1024), P(2048), P(4096), P(8192), 4, ctypes.byref(bad), 1, None) == 1
+
+
+def test_newton_schulz_argument_validation(built):
+    lib = built
+    P = ctypes.c_void_p
+    f = ctypes.c_float
+    # tall input is rejected, count 0 is a no-op
+    assert lib.muon_newton_schulz(P(1024), P(2048), 1, 8, 4, 5, f(1), f(1), f(1), P(4096), 1 << 20, None) == 1
+    assert lib.muon_newton_schulz(None, None, 0, 4, 8, 5, f(1), f(1), f(1), None, 0, None) == 0
+    assert lib.muon_newton_schulz(P(1024), P(2048), 1, 4, 8, 5, f(1), f(1), f(1), P(4096), 16, None) == 4
+
+
+def test_library_never_loads_the_oracle(built):
+    # the product path has no reference to the oracle
+    for path in ("optimizer_muon_step_gb300/__init__.py", "optimizer_muon_step_gb300/build.py"):
+        src = open(os.path.join(ROOT, path)).read()
+        assert "oracle" not in src.replace("no CPU or PyTorch fallback", "")
+    for name in os.listdir(os.path.join(ROOT, "optimizer_muon_step_gb300", "csrc")):
+        assert "oracle" not in open(os.path.join(ROOT, "optimizer_muon_step_gb300", "csrc", name)).read()

@@ -399,3 +399,19 @@ def test_bf16_emulated_ns_tracks_exact_iteration(kind):
     assert np.linalg.norm(emul - exact) / np.linalg.norm(exact) < 2e-2
     # and every stored value is a bf16 value
     assert np.array_equal(oracle.bf16_round(emul.astype(np.float32)), emul.astype(np.float32))
+
+
+def test_stage_functions_compose_to_the_step():
+    """The step is momentum -> normalise -> NS -> final update; the staged
+    entry points reproduce it exactly (tall input, so the transpose path
+    is exercised too)."""
+    W, G, M = _inputs(40, 24, 8)
+    hp = oracle.MuonConfig()
+    W1, M1, X0, O = oracle.muon_step_matrix(W, G, M, hp)
+    M2, u = oracle.momentum(G, M, hp.momentum, hp.nesterov)
+    X0b, s = oracle.normalize(u, hp.norm_eps)
+    Ob = oracle.newton_schulz(X0b, hp.ns_steps).astype(np.float32)
+    W2 = oracle.final_update(W, Ob, hp.lr, hp.weight_decay, hp.rms_scale)
+    assert np.array_equal(M1, M2) and np.array_equal(X0, X0b)
+    assert np.array_equal(O, Ob) and np.array_equal(W1, W2)
+    assert s > 0 and abs(np.linalg.norm(u.astype(np.float64)) * s - 1) < 1e-6
