@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark of the Muon optimizer step on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2]
+    python bench.py --impl reference ...      (the CPU oracle as the reference arm)
+
+A step is one call of muon_step_batched over every hidden matrix of the
+workload (default c2: dense 24-layer decoder, hidden 2048, FFN 5632, 168
+matrices, bf16 gradients): momentum, normalisation, five Newton-Schulz
+iterations on the tensor cores and the final update.  The AdamW step (the
+last row of the hot path) is timed in the same run on the full-size
+embedding + LM-head buffers of the mixed workload (2 x 163840 x 7168 fp32)
+and reported under "adamw".
+
+value: Newton-Schulz TFLOP/s over the whole step time, counting the
+algorithmic flops (symmetry exploited) 3 m'^2 n' + m'^3 per matrix per
+iteration, summed over all ranks; ms_per_step is the Muon step time.
+Under torchrun every rank runs its own replica of the workload (weak
+scaling, no collective on the data path).  Inputs total > 12 GB, larger
+than L2 (129 MB), so no explicit flush is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "Muon optimizer-step ms & NS TFLOP/s (frac of BF16 peak); AdamW HBM GB/s"
+UNIT = "TFLOP/s"
+ADAMW_BYTES_PER_PARAM = 28  # read p, g, m, v (16 B), write p, m, v (12 B)
+KINDS = ("momentum_norm", "norm_finalize", "normalize_cast", "ns_syrk", "ns_poly", "ns_update",
+         "final_update", "adamw")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c2", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--budget-gb", type=float, default=16.0, help="NS workspace budget")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-adamw", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# flop and byte accounting
+# --------------------------------------------------------------------------
+
+def ns_stage_flops(mp: int, np_: int):
+    """Algorithmic flops of one NS iteration on one matrix, per stage."""
+    return {"ns_syrk": mp * (mp + 1) * np_,      # upper triangle of X X^T
+            "ns_poly": mp * mp * (mp + 1),       # upper triangle of A A
+            "ns_update": 2 * mp * mp * np_}      # B X
+
+
+def workload_flops(w: workloads.Workload, steps: int):
+    per = {"ns_syrk": 0, "ns_poly": 0, "ns_update": 0}
+    dense = 0
+    for s in w.matrices:
+        mp, np_ = min(s.rows, s.cols), max(s.rows, s.cols)
+        for k, v in ns_stage_flops(mp, np_).items():
+            per[k] += steps * v
+        dense += steps * (4 * mp * mp * np_ + 2 * mp ** 3)
+    return per, dense
+
+
+def elementwise_bytes(w: workloads.Workload):
+    """Algorithmic HBM bytes per step of the element-wise Muon stages."""
+    out = {"momentum_norm": 0, "normalize_cast": 0, "final_update": 0}
+    for s in w.matrices:
+        n = s.rows * s.cols
+        g = 2 if s.g_dtype.itemsize == 2 else 4
+        out["momentum_norm"] += n * (g + 4 + 4)        # read G, M; write M
+        out["normalize_cast"] += n * (g + 4 + 2)       # read G, M; write X0
+        out["final_update"] += n * (4 + 2 + 4)         # read W, O; write W
+    return out
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sms, maxes, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(self.NAMES, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle (baseline and reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_sample(w: workloads.Workload):
+    """A bounded sample of the workload for the CPU oracle: its most common
+    matrix shape, one matrix, drawn from the workload's distributions."""
+    import collections
+    shapes = collections.Counter((s.rows, s.cols) for s in w.matrices)
+    (rows, cols), _ = shapes.most_common(1)[0]
+    idx = next(i for i, s in enumerate(w.matrices) if (s.rows, s.cols) == (rows, cols))
+    t = workloads.make_muon(w, device="cpu", indices=[idx])
+    mp, np_ = min(rows, cols), max(rows, cols)
+    flops = sum(ns_stage_flops(mp, np_).values()) * workloads.MUON_HPARAMS["ns_steps"]
+    return (t.W[0].numpy(), t.G[0].float().numpy(), t.M[0].numpy()), flops, f"1 matrix {rows}x{cols}"
+
+
+def time_oracle(w: workloads.Workload, repeats: int = 1):
+    import oracle
+    (W, G, M), flops, desc = oracle_sample(w)
+    cfg = oracle.MuonConfig(**workloads.MUON_HPARAMS)
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.muon_step_matrix(W, G, M, cfg)
+        times.append(time.perf_counter() - t0)
+    return times, flops, desc, oracle.num_threads()
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    w = workloads.get(args.workload)
+    _, _, _, cores = time_oracle(workloads.get("c1"))  # build + warm the library
+    for _ in range(args.warmup):
+        time_oracle(w)
+    times, flops, desc, cores = time_oracle(w, repeats=args.steps)
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    sample = f"{desc} of {len(w.matrices)} per step (full Muon step incl. 5 NS iterations)"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.description}", "parallelism": "replicas"},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import optimizer_muon_step_gb300 as m
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    m.load_library()
+    peaks = measured_peaks()
+    w = workloads.get(args.workload)
+    hp = m.MuonHparams(**workloads.MUON_HPARAMS)
+    steps_ns = hp.ns_steps
+    tens = workloads.make_muon(w, device=dev)
+    batch = m.MuonBatch(tens.W, tens.G, tens.M, budget_bytes=int(args.budget_gb * 2 ** 30))
+    stage_flops, dense_flops = workload_flops(w, steps_ns)
+    step_flops = sum(stage_flops.values())
+    ew_bytes = elementwise_bytes(w)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        batch.step(hp, stream)
+    torch.cuda.synchronize()
+    if m.muon_query_status(batch.workspace) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---- device-timed region ----
+    clocks = ClockSampler(local_rank)
+    m.muon_set_timing(True)
+    launches0 = m.muon_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        batch.step(hp, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    launches = m.muon_launch_count() - launches0
+    kernel_times = m.muon_timing_read()
+    m.muon_set_timing(False)
+    status = m.muon_query_status(batch.workspace)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1))
+    ms_step = ms_total / args.steps
+    value = step_flops * args.steps * world / (ms_total / 1e3) / 1e12
+
+    # ---- per-kernel roofline (live, same timed region) ----
+    stages = {}
+    for k in KINDS:
+        ms_k, n_k = kernel_times.get(k, (0.0, 0))
+        if n_k:
+            stages[k] = {"ms_per_step": ms_k / args.steps, "launches_per_step": n_k / args.steps}
+    ns_kinds = [k for k in ("ns_syrk", "ns_poly", "ns_update") if k in stages]
+    dominant = max(stages, key=lambda k: stages[k]["ms_per_step"])
+    for k in ns_kinds:
+        s = stages[k]
+        s["tflops"] = stage_flops[k] / (s["ms_per_step"] / 1e3) / 1e12
+    for k in ("momentum_norm", "normalize_cast", "final_update"):
+        if k in stages:
+            stages[k]["gbs"] = ew_bytes[k] / (stages[k]["ms_per_step"] / 1e3) / 1e9
+    d = stages[dominant]
+    if dominant in ns_kinds:
+        per_launch = stage_flops[dominant] / d["launches_per_step"]
+        ms_launch = d["ms_per_step"] / d["launches_per_step"]
+        achieved = per_launch / (ms_launch / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_kind": f"bf16 sustained, {peaks['source']}",
+                    "algorithmic_per_launch": per_launch, "ms_per_launch": ms_launch,
+                    "traffic": None}
+    else:
+        per_launch = ew_bytes[dominant] / d["launches_per_step"]
+        ms_launch = d["ms_per_step"] / d["launches_per_step"]
+        achieved = per_launch / (ms_launch / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "peak_kind": f"HBM copy, {peaks['source']}",
+                    "algorithmic_per_launch": per_launch, "ms_per_launch": ms_launch, "traffic": None}
+    ns_ms = sum(stages[k]["ms_per_step"] for k in ns_kinds)
+    ns_summary = {"ms_per_step": ns_ms,
+                  "tflops_algorithmic": step_flops / (ns_ms / 1e3) / 1e12,
+                  "tflops_dense_equivalent": dense_flops / (ns_ms / 1e3) / 1e12,
+                  "frac_of_peak_algorithmic": step_flops / (ns_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
+                  "frac_of_peak_dense_equivalent": dense_flops / (ns_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"]}
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        host = [t.cpu().pin_memory() for t in tens.storage]
+        Wf, Gf, Mf = tens.storage
+        h2d = sum(t.numel() * t.element_size() for t in tens.storage)
+        d2h = Wf.numel() * Wf.element_size() + Mf.numel() * Mf.element_size()
+        n_e2e = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            Wf.copy_(host[0], non_blocking=True)
+            Gf.copy_(host[1], non_blocking=True)
+            Mf.copy_(host[2], non_blocking=True)
+            batch.step(hp, stream)
+            host[0].copy_(Wf, non_blocking=True)
+            host[2].copy_(Mf, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / n_e2e
+        e2e = {"value": step_flops * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": n_e2e}
+        del host
+
+    # ---- AdamW on the mixed workload's embedding + LM head ----
+    adamw = None
+    if not args.no_adamw:
+        c5 = workloads.get("c5")
+        ahp = m.AdamwHparams(**workloads.ADAMW_HPARAMS)
+        bufs = [workloads.make_adamw(r * c, seed=c5.seed + i, device=dev)
+                for i, (r, c) in enumerate(c5.adamw_shapes)]
+        n_params = sum(b.p.numel() for b in bufs)
+        for _ in range(args.warmup):
+            for b in bufs:
+                m.adamw_step(b.p, b.g, b.m, b.v, ahp, workloads.ADAMW_STEP, stream)
+        torch.cuda.synchronize()
+        m.muon_set_timing(True)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            for b in bufs:
+                m.adamw_step(b.p, b.g, b.m, b.v, ahp, workloads.ADAMW_STEP, stream)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        at = m.muon_timing_read()["adamw"]
+        m.muon_set_timing(False)
+        a_ms = a0.elapsed_time(a1) / args.steps
+        gbs = ADAMW_BYTES_PER_PARAM * n_params / (a_ms / 1e3) / 1e9
+        k_ms = at[0] / at[1]
+        k_gbs = ADAMW_BYTES_PER_PARAM * (n_params / len(bufs)) / (k_ms / 1e3) / 1e9
+        adamw = {"workload": "c5 AdamW: embedding + LM head, 2 x 163840x7168 fp32, t=100",
+                 "params": n_params, "ms_per_step": a_ms, "gbs": gbs,
+                 "frac_of_hbm": gbs / peaks["hbm_gbs"], "frac_of_nominal_8tbs": gbs / 8000.0,
+                 "kernel_ms_per_launch": k_ms, "kernel_gbs": k_gbs,
+                 "bytes_per_param": ADAMW_BYTES_PER_PARAM}
+        del bufs
+
+    # ---- CPU oracle baseline (rank 0, one GPU only) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times, flops, desc, cores = time_oracle(w, repeats=1)
+        cpu = {"value": flops / times[0] / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{desc} of {len(w.matrices)} (full Muon step, 5 NS iterations), "
+                         f"{times[0]:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": f"{w.name}: {w.description}", "matrices": len(w.matrices),
+                           "muon_params": w.muon_params, "ns_steps": steps_ns,
+                           "ns_flops_per_step_algorithmic": step_flops,
+                           "ns_flops_per_step_dense_equivalent": dense_flops,
+                           "l2": "inputs > 12 GB exceed the 129 MB L2; no flush needed",
+                           "parallelism": "replicas" if world > 1 else "single"},
+                "roofline": roofline, "ns": ns_summary, "stages": stages, "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": launches, "clocks": clk, "adamw": adamw}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

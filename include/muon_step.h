@@ -157,6 +157,38 @@ muon_status_t adamw_step(float* p, const float* g, float* m, float* v,
  * `workspace`; returns MUON_OK or the recorded error (MUON_ERR_TIMEOUT). */
 muon_status_t muon_query_status(void* workspace, void* stream);
 
+/* ---- Instrumentation (no counterpart on the pages) --------------------- */
+
+/* Kernel kinds the library launches. */
+typedef enum {
+    MUON_KERNEL_MOMENTUM_NORM = 0,  /* momentum, look-ahead, sum of squares */
+    MUON_KERNEL_NORM_FINALIZE = 1,  /* per-matrix norm scale                */
+    MUON_KERNEL_NORMALIZE_CAST = 2, /* X0 = bf16(u * s), wide orientation   */
+    MUON_KERNEL_NS_SYRK = 3,        /* A = X X^T                            */
+    MUON_KERNEL_NS_POLY = 4,        /* B = b A + c A A                      */
+    MUON_KERNEL_NS_UPDATE = 5,      /* X = a X + B X                        */
+    MUON_KERNEL_FINAL_UPDATE = 6,   /* W -= lr (wd W + scale O)             */
+    MUON_KERNEL_ADAMW = 7,          /* AdamW                                */
+    MUON_KERNEL_COUNT = 8
+} muon_kernel_kind_t;
+
+/* Process-wide count of kernels this library has launched (all kinds). */
+int64_t muon_launch_count(void);
+
+/* enable != 0: from now on every launch is bracketed by two CUDA events
+ * recorded on its stream (library-owned events; the launches themselves are
+ * unchanged).  Enabling or disabling drops the records collected so far. */
+muon_status_t muon_set_timing(int32_t enable);
+
+/* Waits for the recorded events, writes the summed milliseconds and the
+ * number of launches per muon_kernel_kind_t into the host arrays (nkinds
+ * entries, kinds beyond MUON_KERNEL_COUNT get 0) and drops the records. */
+muon_status_t muon_timing_read(double* ms_per_kind, int64_t* launches_per_kind,
+                               int32_t nkinds);
+
+/* Static name of a kernel kind ("ns_update", ...). */
+const char* muon_kernel_name(int32_t kind);
+
 /* Static description of a status code. */
 const char* muon_status_string(muon_status_t status);
 

@@ -38,7 +38,10 @@ STATUS = {0: "MUON_OK", 1: "MUON_ERR_INVALID_ARG", 2: "MUON_ERR_UNSUPPORTED_DTYP
 # Every symbol include/muon_step.h declares.
 EXPORTS = ("muon_workspace_bytes_per_matrix", "muon_workspace_size", "muon_plan",
            "muon_step_batched", "muon_newton_schulz", "adamw_step", "muon_query_status",
-           "muon_status_string", "muon_version")
+           "muon_status_string", "muon_version", "muon_launch_count", "muon_set_timing",
+           "muon_timing_read", "muon_kernel_name")
+KERNEL_KINDS = ("momentum_norm", "norm_finalize", "normalize_cast", "ns_syrk", "ns_poly",
+                "ns_update", "final_update", "adamw")
 
 
 class MuonError(RuntimeError):
@@ -139,6 +142,14 @@ def load_library(path: str = LIB_PATH):
         lib.muon_status_string.restype = ctypes.c_char_p
         lib.muon_version.argtypes = []
         lib.muon_version.restype = i32
+        lib.muon_launch_count.argtypes = []
+        lib.muon_launch_count.restype = i64
+        lib.muon_set_timing.argtypes = [i32]
+        lib.muon_set_timing.restype = ctypes.c_int
+        lib.muon_timing_read.argtypes = [P, P, i32]
+        lib.muon_timing_read.restype = ctypes.c_int
+        lib.muon_kernel_name.argtypes = [i32]
+        lib.muon_kernel_name.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -289,3 +300,65 @@ def muon_query_status(workspace, stream=None) -> int:
 
 def version() -> int:
     return int(load_library().muon_version())
+
+
+# --------------------------------------------------------------------------
+# Instrumentation
+# --------------------------------------------------------------------------
+
+def muon_launch_count() -> int:
+    """Kernels this library has launched in this process."""
+    return int(load_library().muon_launch_count())
+
+
+def muon_set_timing(enable: bool) -> None:
+    _check(load_library().muon_set_timing(1 if enable else 0), "muon_set_timing")
+
+
+def muon_timing_read() -> dict:
+    """{kernel name: (total ms, launches)} since timing was enabled."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _check(load_library().muon_timing_read(ms, cnt, n), "muon_timing_read")
+    return {KERNEL_KINDS[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+class MuonBatch:
+    """A fixed list of (W, G, M) matrices marshalled once for repeated steps.
+
+    The tensors must stay alive and keep their storage while the batch is
+    used; ``step`` then only passes the prepared array to the library."""
+
+    def __init__(self, W, G, M, budget_bytes: int = 16 << 30, workspace=None):
+        import torch
+        n = len(W)
+        if not (len(G) == n and len(M) == n):
+            raise ValueError("W, G, M must have the same length")
+        self._keep = (list(W), list(G), list(M))
+        self.count = n
+        self.arr = (MuonMatrix * max(1, n))()
+        for i in range(n):
+            w = _dev_tensor(W[i], f"W[{i}]", (torch.float32,))
+            g = _dev_tensor(G[i], f"G[{i}]", (torch.float32, torch.bfloat16))
+            m = _dev_tensor(M[i], f"M[{i}]", (torch.float32,))
+            if w.dim() != 2 or w.shape != g.shape or w.shape != m.shape:
+                raise ValueError(f"matrix {i}: W, G, M must be equal-shaped 2-D tensors")
+            self.arr[i].W, self.arr[i].G, self.arr[i].M = w.data_ptr(), g.data_ptr(), m.data_ptr()
+            self.arr[i].rows, self.arr[i].cols = w.shape
+            self.arr[i].g_dtype = MUON_BF16 if g.dtype == torch.bfloat16 else MUON_F32
+        lib = load_library()
+        if workspace is None:
+            need = ctypes.c_size_t(0)
+            _check(lib.muon_workspace_size(ctypes.cast(self.arr, ctypes.c_void_p), n, int(budget_bytes),
+                                           ctypes.byref(need)), "muon_workspace_size")
+            workspace = allocate_workspace(need.value, W[0].device if n else None)
+        self.workspace = workspace
+
+    def step(self, hp: MuonHparams = MuonHparams(), stream=None):
+        h = hp._c()
+        _check(load_library().muon_step_batched(ctypes.cast(self.arr, ctypes.c_void_p), self.count,
+                                                ctypes.byref(h),
+                                                ctypes.c_void_p(self.workspace.data_ptr()),
+                                                self.workspace.numel(), _stream(stream)),
+               "muon_step_batched")

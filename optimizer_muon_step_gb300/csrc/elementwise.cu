@@ -358,14 +358,18 @@ cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles,
                                  cudaStream_t st) {
     for (int off = 0; off < count; off += 65535) {
         int n = count - off < 65535 ? count - off : 65535;
+        launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
         momentum_norm_kernel<<<dim3(max_tiles, n), kThreads, 0, st>>>(descs + off, s);
+        launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, cudaStream_t st) {
     const int per = kThreads / 32;
+    launch_begin(MUON_KERNEL_NORM_FINALIZE, st);
     norm_finalize_kernel<<<(count + per - 1) / per, kThreads, 0, st>>>(descs, count, eps);
+    launch_end(MUON_KERNEL_NORM_FINALIZE, st);
     return cudaGetLastError();
 }
 
@@ -376,7 +380,9 @@ cudaError_t launch_normalize_cast(const MatDesc* descs, int count, int64_t max_r
     if (gy > 65535u) return cudaErrorInvalidValue;
     for (int off = 0; off < count; off += 65535) {
         int n = count - off < 65535 ? count - off : 65535;
+        launch_begin(MUON_KERNEL_NORMALIZE_CAST, st);
         normalize_cast_kernel<<<dim3(gx, gy, n), kThreads, 0, st>>>(descs + off, s);
+        launch_end(MUON_KERNEL_NORMALIZE_CAST, st);
     }
     return cudaGetLastError();
 }
@@ -388,7 +394,9 @@ cudaError_t launch_final_update(const MatDesc* descs, int count, int64_t max_row
     if (gy > 65535u) return cudaErrorInvalidValue;
     for (int off = 0; off < count; off += 65535) {
         int n = count - off < 65535 ? count - off : 65535;
+        launch_begin(MUON_KERNEL_FINAL_UPDATE, st);
         final_update_kernel<<<dim3(gx, gy, n), kThreads, 0, st>>>(descs + off, s);
+        launch_end(MUON_KERNEL_FINAL_UPDATE, st);
     }
     return cudaGetLastError();
 }
@@ -402,14 +410,18 @@ cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n
     if (aligned) {
         const int64_t nvec = n / 4;
         if (nvec > 0) {
+            launch_begin(MUON_KERNEL_ADAMW, st);
             adamw_vec_kernel<<<grid_for(nvec, kThreads, cap), kThreads, 0, st>>>(
                 reinterpret_cast<float4*>(p), reinterpret_cast<const float4*>(g),
                 reinterpret_cast<float4*>(m), reinterpret_cast<float4*>(v), nvec, s);
+            launch_end(MUON_KERNEL_ADAMW, st);
         }
         done = nvec * 4;
     }
     if (done < n) {
+        launch_begin(MUON_KERNEL_ADAMW, st);
         adamw_scalar_kernel<<<grid_for(n - done, kThreads, cap), kThreads, 0, st>>>(p, g, m, v, done, n, s);
+        launch_end(MUON_KERNEL_ADAMW, st);
     }
     return cudaGetLastError();
 }

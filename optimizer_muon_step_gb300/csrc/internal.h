@@ -49,6 +49,12 @@ struct AdamwScalars {
     float bc1, bc2, eps, weight_decay;
 };
 
+// ---- launch accounting (timing.cu) -----------------------------------------
+// Every kernel launch is bracketed by launch_begin / launch_end: they count
+// launches and, when timing is enabled, record CUDA events on the stream.
+void launch_begin(int kind, cudaStream_t st);
+void launch_end(int kind, cudaStream_t st);
+
 // ---- element-wise kernels (elementwise.cu) --------------------------------
 cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles,
                                  MomentumScalars s, cudaStream_t st);

@@ -640,7 +640,11 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, f
     }
     if (tiles == 0) return cudaSuccess;
     const int grid = tiles < num_sms ? tiles : num_sms;
+    constexpr int kind = MODE == MODE_SYRK ? MUON_KERNEL_NS_SYRK
+                         : MODE == MODE_POLY ? MUON_KERNEL_NS_POLY : MUON_KERNEL_NS_UPDATE;
+    launch_begin(kind, st);
     ns_gemm_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(prm);
+    launch_end(kind, st);
     return cudaGetLastError();
 }
 
