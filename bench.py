@@ -91,6 +91,23 @@ def elementwise_bytes(w: workloads.Workload):
     return out
 
 
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity on one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_per_step: int, steps: int, world: int, ms_total_max: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of the workload
+    (weak scaling), timed by the slowest rank."""
+    return flops_per_step * steps * world / (ms_total_max / 1e3) / 1e12
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -239,11 +256,7 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, world, dev)
 
     for _ in range(args.warmup):
         batch.step(hp, stream)
@@ -274,7 +287,7 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {status} after the timed region")
     ms_total = max_over_ranks(ev0.elapsed_time(ev1))
     ms_step = ms_total / args.steps
-    value = step_flops * args.steps * world / (ms_total / 1e3) / 1e12
+    value = aggregate_tflops(step_flops, args.steps, world, ms_total)
 
     # ---- per-kernel roofline (live, same timed region) ----
     stages = {}
