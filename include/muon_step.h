@@ -129,6 +129,35 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count,
                                 const muon_hparams_t* hp, void* workspace,
                                 size_t ws_bytes, void* stream);
 
+/* Size of the library-owned device scratch used by muon_step_batched_noalloc:
+ * 64 MiB on every GPU where the library's device code is loaded, held until
+ * the process exits. */
+#define MUON_STATIC_SCRATCH_BYTES (64u << 20)
+
+/* The same Muon step as muon_step_batched, for callers that cannot allocate
+ * device memory (e.g. an optimizer plug-in inside a framework that owns all
+ * device memory through its own pool, or a C caller with no device
+ * allocator): the workspace is a static device array inside the library,
+ * so this call allocates nothing -- no cudaMalloc, no cudaFree, no
+ * allocating library routine.  The pages have no counterpart; it is an
+ * interface variant of the step above.  The caller still passes every
+ * W, G, M buffer.
+ *   - every matrix must fit the scratch on its own:
+ *     muon_workspace_bytes_per_matrix(rows, cols) <= MUON_STATIC_SCRATCH_BYTES
+ *     (e.g. up to 2048 x 5632), else MUON_ERR_WORKSPACE_TOO_SMALL and
+ *     nothing is enqueued; larger call lists run in several passes;
+ *   - the first call on a device resolves the scratch's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first
+ *     call before any stream capture;
+ *   - all calls on a device share the one scratch, which keeps the previous
+ *     call's contents (the step rewrites everything it reads, and clears its
+ *     status word itself): calls that overlap on the GPU (other streams,
+ *     other threads) race and must be serialised by the caller;
+ *   - the status word of a timed-out wait lands in the scratch, which the
+ *     caller cannot address: muon_query_status does not apply. */
+muon_status_t muon_step_batched_noalloc(const muon_matrix_t* mats, int64_t count,
+                                        const muon_hparams_t* hp, void* stream);
+
 /* Newton-Schulz alone on a batch of `count` wide bf16 matrices (device,
  * [count][mp][np] row-major, bf16 bit patterns, mp <= np), writing the
  * result to X_out (same layout; may not alias X_in):

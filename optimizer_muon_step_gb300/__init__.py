@@ -39,7 +39,7 @@ STATUS = {0: "MUON_OK", 1: "MUON_ERR_INVALID_ARG", 2: "MUON_ERR_UNSUPPORTED_DTYP
 EXPORTS = ("muon_workspace_bytes_per_matrix", "muon_workspace_size", "muon_plan",
            "muon_step_batched", "muon_newton_schulz", "adamw_step", "muon_query_status",
            "muon_status_string", "muon_version", "muon_launch_count", "muon_set_timing",
-           "muon_timing_read", "muon_kernel_name")
+           "muon_timing_read", "muon_kernel_name", "muon_step_batched_noalloc")
 KERNEL_KINDS = ("momentum_norm", "norm_finalize", "normalize_cast", "ns_syrk", "ns_poly",
                 "ns_update", "final_update", "adamw")
 
@@ -131,6 +131,8 @@ def load_library(path: str = LIB_PATH):
         lib.muon_plan.restype = ctypes.c_int
         lib.muon_step_batched.argtypes = [P, i64, P, P, ctypes.c_size_t, P]
         lib.muon_step_batched.restype = ctypes.c_int
+        lib.muon_step_batched_noalloc.argtypes = [P, i64, P, P]
+        lib.muon_step_batched_noalloc.restype = ctypes.c_int
         lib.muon_newton_schulz.argtypes = [P, P, i64, i64, i64, i32, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_float, P, ctypes.c_size_t, P]
         lib.muon_newton_schulz.restype = ctypes.c_int
@@ -252,6 +254,31 @@ def muon_step_batched(W, G, M, hp: MuonHparams = MuonHparams(), workspace=None, 
                                  ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                                  _stream(stream)), "muon_step_batched")
     return workspace
+
+
+def muon_step_batched_noalloc(W, G, M, hp: MuonHparams = MuonHparams(), stream=None):
+    """The Muon step with the library's static device scratch as workspace:
+    no device memory is allocated by this call or by the library.  For
+    callers that cannot allocate; every matrix must fit the 64 MiB scratch
+    on its own, and calls that overlap on the GPU race on that scratch."""
+    import torch
+    n = len(W)
+    if not (len(G) == n and len(M) == n):
+        raise ValueError("W, G, M must have the same length")
+    arr = (MuonMatrix * max(1, n))()
+    for i in range(n):
+        w = _dev_tensor(W[i], f"W[{i}]", (torch.float32,))
+        g = _dev_tensor(G[i], f"G[{i}]", (torch.float32, torch.bfloat16))
+        m = _dev_tensor(M[i], f"M[{i}]", (torch.float32,))
+        if w.dim() != 2 or w.shape != g.shape or w.shape != m.shape:
+            raise ValueError(f"matrix {i}: W, G, M must be equal-shaped 2-D tensors")
+        arr[i].W, arr[i].G, arr[i].M = w.data_ptr(), g.data_ptr(), m.data_ptr()
+        arr[i].rows, arr[i].cols = w.shape
+        arr[i].g_dtype = MUON_BF16 if g.dtype == torch.bfloat16 else MUON_F32
+    h = hp._c()
+    _check(load_library().muon_step_batched_noalloc(ctypes.cast(arr, ctypes.c_void_p), n,
+                                                    ctypes.byref(h), _stream(stream)),
+           "muon_step_batched_noalloc")
 
 
 def muon_newton_schulz(X, steps: int = 5, coeffs=(3.4445, -4.7750, 2.0315), out=None,
