@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--subset", type=int, default=0,
+                    help="profiling only: keep the first N matrices of the workload")
     return ap.parse_args()
 
 
@@ -243,6 +245,9 @@ def run_ours(args, rank, world, local_rank):
     m.load_library()
     peaks = measured_peaks()
     w = workloads.get(args.workload)
+    if args.subset:
+        w.matrices = w.matrices[:args.subset]
+        w.description += f" (first {args.subset} matrices only, profiling subset)"
     hp = m.MuonHparams(**workloads.MUON_HPARAMS)
     steps_ns = hp.ns_steps
     tens = workloads.make_muon(w, device=dev)

@@ -47,9 +47,20 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
+#ifndef MUON_EPI_WARPS
+#define MUON_EPI_WARPS 4
+#endif
+#ifndef MUON_PF_UPDATE
+#define MUON_PF_UPDATE 0
+#endif
+#ifndef MUON_PF_SYM
+#define MUON_PF_SYM 3
+#endif
+constexpr int EPI_WARPS = MUON_EPI_WARPS;  // 4 or 8; two warps per TMEM lane quarter when 8
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;  // two BN-column fp32 accumulators
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int XPOSE_BYTES = EPI_WARPS * 16 * 33 * 4;  // per-warp transpose buffers of the epilogue warps
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XPOSE_BYTES + 256;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 enum Mode { MODE_SYRK = 0, MODE_POLY = 1, MODE_UPDATE = 2 };
@@ -266,6 +277,149 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // ---------------------------------------------------------------------------
+// Epilogue of one tile, run by one warp over its 32 TMEM lanes (rows) and
+// the tile's 8 chunks of 32 columns.
+// ---------------------------------------------------------------------------
+constexpr int XPOSE_WORDS = 16 * 33;  // per-warp 32x32 bf16 transpose buffer
+
+// Chunk values packed as bf16 pairs, w[i] = columns (2i, 2i+1):
+//   SYRK  acc;   POLY  alpha*E + beta*acc;   UPDATE  alpha*E + acc
+template <int MODE>
+__device__ __forceinline__ void chunk_values(const float (&v)[32], const uint4 (&e)[4], float alpha, float beta,
+                                             uint32_t (&w)[16]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t ew[4] = {e[q].x, e[q].y, e[q].z, e[q].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int i = q * 4 + h;
+            float lo = v[2 * i], hi = v[2 * i + 1];
+            if (MODE == MODE_POLY) {
+                lo = __fadd_rn(__fmul_rn(alpha, bf16_lo(ew[h])), __fmul_rn(beta, lo));
+                hi = __fadd_rn(__fmul_rn(alpha, bf16_hi(ew[h])), __fmul_rn(beta, hi));
+            } else if (MODE == MODE_UPDATE) {
+                lo = __fadd_rn(__fmul_rn(alpha, bf16_lo(ew[h])), lo);
+                hi = __fadd_rn(__fmul_rn(alpha, bf16_hi(ew[h])), hi);
+            }
+            w[i] = pack_bf16x2(lo, hi);
+        }
+    }
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
+// Waits for the accumulator, then writes the tile.  The addend (E) of the
+// first three chunks is requested before the wait and each later chunk's
+// three chunks ahead, so its latency overlaps the main loop and the
+// previous chunks.  Chunks strictly above the diagonal (or any chunk in
+// UPDATE) with full rows and columns take the vector path; SYRK/POLY write
+// their mirror block through a per-warp shared-memory transpose with 16-byte
+// stores.  Returns false when the CTA is aborting.
+template <int MODE>
+__device__ __forceinline__ bool epilogue_tile(const NsParams& p, const GroupParams& g, const Tile& tile,
+                                              uint32_t t_acc, int quarter, int half, int lane, uint32_t* xpose,
+                                              uint32_t tfull, uint32_t acc_phase, volatile int* abort_flag) {
+    constexpr int CH = BN / 32 / (EPI_WARPS / 4);  // chunks of 32 columns this warp writes
+    constexpr int PF = (MODE == MODE_UPDATE) ? MUON_PF_UPDATE : MUON_PF_SYM;  // addend prefetch depth
+    const int row_base = tile.ti * BM + quarter * 32;
+    const int row = row_base + lane;
+    const bool row_ok = row < g.M;
+    const int64_t mat_off = static_cast<int64_t>(tile.mat) * g.bs;
+    uint16_t* __restrict__ D = g.D + mat_off;
+    const uint16_t* __restrict__ E = (MODE == MODE_SYRK) ? nullptr : g.E + mat_off;
+    uint16_t* drow = D + static_cast<int64_t>(row) * g.ld;
+    const uint16_t* erow = (MODE == MODE_SYRK) ? nullptr : E + static_cast<int64_t>(row) * g.ld;
+    const int col_base = tile.tj * BN + half * CH * 32;
+    const int N = g.N;
+    const float alpha = p.alpha, beta = p.beta;
+
+    constexpr int RING = PF > 0 ? PF : 1;
+    uint4 ering[RING][4];
+#pragma unroll
+    for (int s = 0; s < RING; ++s)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ering[s][q] = make_uint4(0u, 0u, 0u, 0u);
+    auto prefetch = [&](int c, uint4 (&dst)[4]) {
+        const int col0 = col_base + 32 * c;
+        if (MODE != MODE_SYRK && row_ok && col0 + 32 <= N && (MODE == MODE_UPDATE || col0 + 31 >= row_base)) {
+            const uint4* src = reinterpret_cast<const uint4*>(erow + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = __ldg(src + q);
+        }
+    };
+#pragma unroll
+    for (int c = 0; c < PF && c < CH; ++c) prefetch(c, ering[c]);
+
+    if (!wait_bounded(tfull, acc_phase, abort_flag, p.status)) return false;
+    tc_fence_after();
+    const uint32_t t_addr = t_acc + (static_cast<uint32_t>(quarter * 32) << 16);
+
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        uint4 e[4];
+        if (PF == 0) {
+            prefetch(c, ering[0]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) e[q] = ering[0][q];
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) e[q] = ering[c % RING][q];
+            if (c + PF < CH) prefetch(c + PF, ering[c % RING]);
+        }
+        const int col0 = col_base + 32 * c;
+        if (col0 >= N) continue;                                          // warp-uniform
+        if (MODE != MODE_UPDATE && col0 + 31 < row_base) continue;     // below the diagonal
+        __syncwarp();
+        float v[32];
+        tmem_load_32cols(t_addr + static_cast<uint32_t>((half * CH + c) * 32), v);
+        const bool fast = col0 + 32 <= N && row_base + 32 <= g.M && (MODE == MODE_UPDATE || col0 >= row_base + 32);
+        if (fast) {
+            uint32_t w[16];
+            chunk_values<MODE>(v, e, alpha, beta, w);
+            uint4* dst = reinterpret_cast<uint4*>(drow + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            if (MODE != MODE_UPDATE) {
+                // mirror: rows col0..col0+31, columns row_base..row_base+31
+#pragma unroll
+                for (int i = 0; i < 16; ++i) xpose[i * 33 + lane] = w[i];
+                __syncwarp();
+                const uint32_t* src = xpose + (lane >> 1) * 33;
+                const uint32_t sel = (lane & 1) ? 0x7632u : 0x5410u;
+                uint32_t o[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) o[k] = __byte_perm(src[2 * k], src[2 * k + 1], sel);
+                uint4* mdst = reinterpret_cast<uint4*>(D + static_cast<int64_t>(col0 + lane) * g.ld + row_base);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mdst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                __syncwarp();
+            }
+        } else if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int col = col0 + j;
+                if (col < N) {
+                    float val = v[j];
+                    if (MODE != MODE_SYRK) {
+                        const float ev = __uint_as_float(static_cast<uint32_t>(erow[col]) << 16);
+                        val = (MODE == MODE_POLY) ? __fadd_rn(__fmul_rn(alpha, ev), __fmul_rn(beta, val))
+                                                  : __fadd_rn(__fmul_rn(alpha, ev), val);
+                    }
+                    const uint16_t b = to_bf16(val);
+                    if (MODE == MODE_UPDATE) {
+                        drow[col] = b;
+                    } else {
+                        if (col >= row) drow[col] = b;
+                        if (col > row) D[static_cast<int64_t>(col) * g.ld + row] = b;
+                    }
+                }
+            }
+        }
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 template <int MODE>
@@ -273,7 +427,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tiles = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint32_t* xpose_all = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + XPOSE_BYTES);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + STAGES;
     uint64_t* tfull_bar = bars + 2 * STAGES;
@@ -292,7 +447,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
-            mbar_init(smem_u32(&tempty_bar[a]), 4);
+            mbar_init(smem_u32(&tempty_bar[a]), EPI_WARPS);
         }
         mbar_init(smem_u32(drain_bar), 1);
         *abort_flag = 0;
@@ -398,116 +553,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         wait_bounded(smem_u32(drain_bar), 0, abort_flag, p.status);
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
-        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
+        const int half = (warp - 2) >> 2;    // column half when two warps share a quarter
+        uint32_t* xpose = xpose_all + (warp - 2) * XPOSE_WORDS;
         int local = 0;
         for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
             const Tile tile = decode_tile<MODE>(p, t);
             const GroupParams& g = p.g[tile.group];
             const int acc = local & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
-            if (!wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status)) break;
-            tc_fence_after();
-            const int row_base = tile.ti * BM + quarter * 32;
-            const int row = row_base + lane;
-            const int64_t mat_off = static_cast<int64_t>(tile.mat) * g.bs;
-            uint16_t* __restrict__ D = g.D + mat_off;
-            const uint16_t* __restrict__ E = (MODE == MODE_SYRK) ? nullptr : g.E + mat_off;
-            const uint32_t t_addr = tmem_base + static_cast<uint32_t>(acc * BN) +
-                                    (static_cast<uint32_t>(quarter * 32) << 16);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int col0 = tile.tj * BN + c * 32;
-                if (col0 >= g.N) break;                                        // warp-uniform
-                if (MODE != MODE_UPDATE && col0 + 31 < row_base) continue;   // below diagonal
-                __syncwarp();
-                float v[32];
-                tmem_load_32cols(t_addr + static_cast<uint32_t>(c * 32), v);
-                if (row >= g.M) continue;
-                const bool full_cols = col0 + 32 <= g.N;
-                if (MODE == MODE_UPDATE) {
-                    uint16_t* drow = D + static_cast<int64_t>(row) * g.ld + col0;
-                    const uint16_t* erow = E + static_cast<int64_t>(row) * g.ld + col0;
-                    if (full_cols) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 e = __ldg(reinterpret_cast<const uint4*>(erow) + q);
-                            const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
-                            uint32_t o[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const int j = q * 8 + h * 2;
-                                float lo = __fadd_rn(__fmul_rn(p.alpha, bf16_lo(ew[h])), v[j]);
-                                float hi = __fadd_rn(__fmul_rn(p.alpha, bf16_hi(ew[h])), v[j + 1]);
-                                o[h] = pack_bf16x2(lo, hi);
-                            }
-                            reinterpret_cast<uint4*>(drow)[q] = make_uint4(o[0], o[1], o[2], o[3]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (col0 + j < g.N) {
-                                float e = __uint_as_float(static_cast<uint32_t>(erow[j]) << 16);
-                                float val = __fadd_rn(__fmul_rn(p.alpha, e), v[j]);
-                                drow[j] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-                            }
-                        }
-                    }
-                } else {
-                    // symmetric output: store (row, col) for col >= row and the
-                    // mirror (col, row) for col > row
-                    uint16_t* drow = D + static_cast<int64_t>(row) * g.ld;
-                    const uint16_t* erow = (MODE == MODE_POLY) ? E + static_cast<int64_t>(row) * g.ld : nullptr;
-                    uint16_t out[32];
-                    if (MODE == MODE_POLY && full_cols) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 e = __ldg(reinterpret_cast<const uint4*>(erow + col0) + q);
-                            const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const int j = q * 8 + h * 2;
-                                float lo = __fadd_rn(__fmul_rn(p.alpha, bf16_lo(ew[h])), __fmul_rn(p.beta, v[j]));
-                                float hi = __fadd_rn(__fmul_rn(p.alpha, bf16_hi(ew[h])), __fmul_rn(p.beta, v[j + 1]));
-                                out[j] = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-                                out[j + 1] = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            float val = v[j];
-                            if (MODE == MODE_POLY) {
-                                const int col = col0 + j;
-                                float e = (col < g.N) ? __uint_as_float(static_cast<uint32_t>(erow[col]) << 16) : 0.f;
-                                val = __fadd_rn(__fmul_rn(p.alpha, e), __fmul_rn(p.beta, val));
-                            }
-                            out[j] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-                        }
-                    }
-                    if (full_cols && col0 >= row) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 w;
-                            w.x = out[q * 8 + 0] | (static_cast<uint32_t>(out[q * 8 + 1]) << 16);
-                            w.y = out[q * 8 + 2] | (static_cast<uint32_t>(out[q * 8 + 3]) << 16);
-                            w.z = out[q * 8 + 4] | (static_cast<uint32_t>(out[q * 8 + 5]) << 16);
-                            w.w = out[q * 8 + 6] | (static_cast<uint32_t>(out[q * 8 + 7]) << 16);
-                            reinterpret_cast<uint4*>(drow + col0)[q] = w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int col = col0 + j;
-                            if (col < g.N && col >= row) drow[col] = out[j];
-                        }
-                    }
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = col0 + j;
-                        if (col < g.N && col > row) D[static_cast<int64_t>(col) * g.ld + row] = out[j];
-                    }
-                }
-            }
+            if (!epilogue_tile<MODE>(p, g, tile, tmem_base + static_cast<uint32_t>(acc * BN), quarter, half, lane, xpose,
+                                     smem_u32(&tfull_bar[acc]), acc_phase, abort_flag))
+                break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
