@@ -50,17 +50,14 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 #ifndef MUON_EPI_WARPS
 #define MUON_EPI_WARPS 4
 #endif
-#ifndef MUON_PF_UPDATE
-#define MUON_PF_UPDATE 0
-#endif
-#ifndef MUON_PF_SYM
-#define MUON_PF_SYM 3
-#endif
 constexpr int EPI_WARPS = MUON_EPI_WARPS;  // 4 or 8; two warps per TMEM lane quarter when 8
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;  // two BN-column fp32 accumulators
-constexpr int XPOSE_BYTES = EPI_WARPS * 16 * 33 * 4;  // per-warp transpose buffers of the epilogue warps
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XPOSE_BYTES + 256;
+constexpr int EBUF_BYTES = 32 * 32 * 2;                  // one 32x32 bf16 block
+constexpr int NSLOT = 4;                                   // block buffers per epilogue warp
+constexpr int EBUFS_BYTES = EPI_WARPS * NSLOT * EBUF_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EBUFS_BYTES + 256;
+constexpr unsigned long long kDrainNs = 500000000ull;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 enum Mode { MODE_SYRK = 0, MODE_POLY = 1, MODE_UPDATE = 2 };
@@ -68,6 +65,9 @@ enum Mode { MODE_SYRK = 0, MODE_POLY = 1, MODE_UPDATE = 2 };
 struct GroupParams {
     CUtensorMap tm_a;      // A operand: rows of the left factor, K-major, box {64, 128}
     CUtensorMap tm_b;      // B operand: K-major box {64, 256} or MN-major box {64, 64}
+    CUtensorMap tm_e;      // epilogue addend, box {32, 32}, 64-byte swizzle
+    CUtensorMap tm_d;      // output block store, box {32, 32}, 64-byte swizzle
+    CUtensorMap tm_m;      // mirror block store, box {32, 32}, no swizzle
     const uint16_t* E;     // epilogue addend (POLY: A, UPDATE: X)
     uint16_t* D;           // output
     int64_t ld;            // row stride of D and E, elements
@@ -146,6 +146,19 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// Bounded wait that ignores the abort flag: used to let copies and MMAs this
+// CTA issued land before it releases TMEM and exits.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kDrainNs) return;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint32_t bar) {
     asm volatile(
@@ -154,6 +167,24 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until at most N committed bulk groups are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until every committed bulk store has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -280,7 +311,6 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // Epilogue of one tile, run by one warp over its 32 TMEM lanes (rows) and
 // the tile's 8 chunks of 32 columns.
 // ---------------------------------------------------------------------------
-constexpr int XPOSE_WORDS = 16 * 33;  // per-warp 32x32 bf16 transpose buffer
 
 // Chunk values packed as bf16 pairs, w[i] = columns (2i, 2i+1):
 //   SYRK  acc;   POLY  alpha*E + beta*acc;   UPDATE  alpha*E + acc
@@ -308,114 +338,174 @@ __device__ __forceinline__ void chunk_values(const float (&v)[32], const uint4 (
 
 __device__ __forceinline__ uint16_t to_bf16(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
-// Waits for the accumulator, then writes the tile.  The addend (E) of the
-// first three chunks is requested before the wait and each later chunk's
-// three chunks ahead, so its latency overlaps the main loop and the
-// previous chunks.  Chunks strictly above the diagonal (or any chunk in
-// UPDATE) with full rows and columns take the vector path; SYRK/POLY write
-// their mirror block through a per-warp shared-memory transpose with 16-byte
-// stores.  Returns false when the CTA is aborting.
+// Per-warp state of the epilogue's bulk copies; lives across tiles.  Each
+// epilogue warp owns NSLOT 2 KB block buffers (64-byte swizzle): the first
+// RING slots hold the addend-in / output-out ring, and for SYRK/POLY slots 2
+// and 3 alternate as mirror staging.
+struct EpiBufs {
+    uint32_t buf[NSLOT];    // shared::cta addresses
+    uint8_t* ptr[NSLOT];    // the same buffers as generic pointers
+    uint32_t bar[NSLOT];    // mbarriers of addend loads into the slots
+    uint32_t phase;         // bit b: parity of the next completion of bar[b]
+    uint32_t pending;       // bit b: an addend load into slot b is in flight
+    uint32_t seq;           // blocks this warp has written so far (all tiles)
+};
+
+// Ring of addend/output slots per stage and how many blocks ahead the
+// addend is loaded (measured on the dense-decoder workload; a slot is
+// reused once the bulk group RING-AHEAD blocks back has been read).
+#ifndef MUON_RING_UPDATE
+#define MUON_RING_UPDATE 2
+#endif
+#ifndef MUON_AHEAD_UPDATE
+#define MUON_AHEAD_UPDATE 2
+#endif
+#ifndef MUON_RING_SYM
+#define MUON_RING_SYM 2
+#endif
+#ifndef MUON_AHEAD_SYM
+#define MUON_AHEAD_SYM 2
+#endif
+template <int MODE>
+struct EpiRing {
+    static constexpr int kRing = MODE == MODE_UPDATE ? MUON_RING_UPDATE : MUON_RING_SYM;
+    static constexpr int kAhead = MODE == MODE_UPDATE ? MUON_AHEAD_UPDATE : MUON_AHEAD_SYM;
+    static_assert(kAhead >= 1 && kAhead <= kRing, "addend distance must fit the ring");
+    static_assert(kRing + (MODE == MODE_UPDATE ? 0 : 2) <= NSLOT, "ring and mirror slots exceed NSLOT");
+};
+
+// Waits for the accumulator, then writes the tile, 32x32 blocks at a time.
+//   addend (POLY: A, UPDATE: X): bulk tensor load into a slot of the ring,
+//     requested kAhead blocks ahead; the first ones before the accumulator
+//     wait so they overlap the main loop;
+//   output: each lane writes its row of the finished block into the same
+//     slot (same swizzle) and one lane issues a bulk tensor store; the
+//     mirror block of SYRK/POLY goes through a transposed staging slot and a
+//     second bulk store in the same bulk group.  Rows or columns past the
+//     matrix are clipped by the tensor store.  A slot is reused only after
+//     the bulk group that read it (two groups back) has finished reading;
+//   diagonal blocks of SYRK/POLY (col0 == row_base) are written element by
+//     element, so each element of the symmetric output has exactly one
+//     writer.
+// Returns false when the CTA is aborting.
 template <int MODE>
 __device__ __forceinline__ bool epilogue_tile(const NsParams& p, const GroupParams& g, const Tile& tile,
-                                              uint32_t t_acc, int quarter, int half, int lane, uint32_t* xpose,
-                                              uint32_t tfull, uint32_t acc_phase, volatile int* abort_flag) {
-    constexpr int CH = BN / 32 / (EPI_WARPS / 4);  // chunks of 32 columns this warp writes
-    constexpr int PF = (MODE == MODE_UPDATE) ? MUON_PF_UPDATE : MUON_PF_SYM;  // addend prefetch depth
+                                              uint32_t t_acc, int quarter, int half, int lane, uint32_t tfull,
+                                              uint32_t acc_phase, volatile int* abort_flag, EpiBufs& eb) {
+    constexpr int CH = BN / 32 / (EPI_WARPS / 4);  // blocks of 32 columns this warp writes
+    constexpr int RING = EpiRing<MODE>::kRing;
+    constexpr int AHEAD = EpiRing<MODE>::kAhead;
     const int row_base = tile.ti * BM + quarter * 32;
     const int row = row_base + lane;
-    const bool row_ok = row < g.M;
     const int64_t mat_off = static_cast<int64_t>(tile.mat) * g.bs;
     uint16_t* __restrict__ D = g.D + mat_off;
-    const uint16_t* __restrict__ E = (MODE == MODE_SYRK) ? nullptr : g.E + mat_off;
-    uint16_t* drow = D + static_cast<int64_t>(row) * g.ld;
-    const uint16_t* erow = (MODE == MODE_SYRK) ? nullptr : E + static_cast<int64_t>(row) * g.ld;
     const int col_base = tile.tj * BN + half * CH * 32;
     const int N = g.N;
     const float alpha = p.alpha, beta = p.beta;
 
-    constexpr int RING = PF > 0 ? PF : 1;
-    uint4 ering[RING][4];
-#pragma unroll
-    for (int s = 0; s < RING; ++s)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ering[s][q] = make_uint4(0u, 0u, 0u, 0u);
-    auto prefetch = [&](int c, uint4 (&dst)[4]) {
-        const int col0 = col_base + 32 * c;
-        if (MODE != MODE_SYRK && row_ok && col0 + 32 <= N && (MODE == MODE_UPDATE || col0 + 31 >= row_base)) {
-            const uint4* src = reinterpret_cast<const uint4*>(erow + col0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = __ldg(src + q);
+    // blocks this warp writes: [c_lo, c_hi), the same for all lanes
+    int c_hi = CH;
+    while (c_hi > 0 && col_base + 32 * (c_hi - 1) >= N) --c_hi;
+    if (row_base >= g.M) c_hi = 0;  // every row of this warp is past the matrix
+    int c_lo = 0;
+    if (MODE != MODE_UPDATE)
+        while (c_lo < c_hi && col_base + 32 * c_lo + 31 < row_base) ++c_lo;  // below the diagonal
+    const int nblocks = c_hi - c_lo;
+
+    // Blocks are numbered across tiles (eb.seq) and block n uses slot
+    // n % RING (mirror slot 2 + n % 2).  Every block commits exactly one bulk
+    // group (possibly empty), so after block n's "at most RING-AHEAD groups
+    // still reading" every slot of blocks <= n-(RING-AHEAD) is free -- in
+    // particular the slot the addend load for block n+AHEAD overwrites, in
+    // this tile or at the start of the next one.
+    const uint32_t s0 = eb.seq;
+    auto issue = [&](int k) {  // addend of the k-th written block of this tile
+        if (MODE == MODE_SYRK) return;
+        const int b = static_cast<int>((s0 + k) % RING);
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_expect_tx(eb.bar[b], EBUF_BYTES);
+            tma_load_3d(eb.buf[b], &g.tm_e, col_base + 32 * (c_lo + k), row_base, tile.mat, eb.bar[b]);
         }
+        eb.pending |= 1u << b;
     };
 #pragma unroll
-    for (int c = 0; c < PF && c < CH; ++c) prefetch(c, ering[c]);
+    for (int k = 0; k < AHEAD; ++k)
+        if (k < nblocks) issue(k);
 
     if (!wait_bounded(tfull, acc_phase, abort_flag, p.status)) return false;
     tc_fence_after();
     const uint32_t t_addr = t_acc + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int sw = (lane >> 1) & 3;  // 64-byte swizzle of this lane's row
 
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-        uint4 e[4];
-        if (PF == 0) {
-            prefetch(c, ering[0]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) e[q] = ering[0][q];
-        } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) e[q] = ering[c % RING][q];
-            if (c + PF < CH) prefetch(c + PF, ering[c % RING]);
-        }
+    for (int k = 0; k < nblocks; ++k) {
+        const int c = c_lo + k;
+        const int b = static_cast<int>((s0 + k) % RING);
+        const int mb = 2 + static_cast<int>((s0 + k) & 1);  // mirror slot (SYRK/POLY)
         const int col0 = col_base + 32 * c;
-        if (col0 >= N) continue;                                          // warp-uniform
-        if (MODE != MODE_UPDATE && col0 + 31 < row_base) continue;     // below the diagonal
         __syncwarp();
         float v[32];
         tmem_load_32cols(t_addr + static_cast<uint32_t>((half * CH + c) * 32), v);
-        const bool fast = col0 + 32 <= N && row_base + 32 <= g.M && (MODE == MODE_UPDATE || col0 >= row_base + 32);
-        if (fast) {
+        uint8_t* brow = eb.ptr[b] + lane * 64;
+        uint4 e[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                      make_uint4(0u, 0u, 0u, 0u)};
+        if (MODE != MODE_SYRK) {
+            if (!wait_bounded(eb.bar[b], (eb.phase >> b) & 1u, abort_flag, p.status)) return false;
+            eb.phase ^= 1u << b;
+            eb.pending &= ~(1u << b);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) e[q] = *reinterpret_cast<const uint4*>(brow + ((q ^ sw) << 4));
+        }
+        const bool diagonal = MODE != MODE_UPDATE && col0 == row_base;
+        if (!diagonal) {
             uint32_t w[16];
             chunk_values<MODE>(v, e, alpha, beta, w);
-            uint4* dst = reinterpret_cast<uint4*>(drow + col0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(brow + ((q ^ sw) << 4)) =
+                    make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
             if (MODE != MODE_UPDATE) {
-                // mirror: rows col0..col0+31, columns row_base..row_base+31
+                // mirror block: element (col0 + j, row_base + lane) at j * 32 + lane
+                uint16_t* mrow = reinterpret_cast<uint16_t*>(eb.ptr[mb]);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) xpose[i * 33 + lane] = w[i];
-                __syncwarp();
-                const uint32_t* src = xpose + (lane >> 1) * 33;
-                const uint32_t sel = (lane & 1) ? 0x7632u : 0x5410u;
-                uint32_t o[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) o[k] = __byte_perm(src[2 * k], src[2 * k + 1], sel);
-                uint4* mdst = reinterpret_cast<uint4*>(D + static_cast<int64_t>(col0 + lane) * g.ld + row_base);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) mdst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-                __syncwarp();
+                for (int i = 0; i < 16; ++i) {
+                    mrow[(2 * i) * 32 + lane] = static_cast<uint16_t>(w[i] & 0xffffu);
+                    mrow[(2 * i + 1) * 32 + lane] = static_cast<uint16_t>(w[i] >> 16);
+                }
             }
-        } else if (row_ok) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(&g.tm_d, eb.buf[b], col0, row_base, tile.mat);
+                if (MODE != MODE_UPDATE) tma_store_3d(&g.tm_m, eb.buf[mb], row_base, col0, tile.mat);
+            }
+        } else if (row < g.M) {
+            uint16_t* drow = D + static_cast<int64_t>(row) * g.ld;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int col = col0 + j;
-                if (col < N) {
+                if (col < N && col >= row) {
                     float val = v[j];
-                    if (MODE != MODE_SYRK) {
-                        const float ev = __uint_as_float(static_cast<uint32_t>(erow[col]) << 16);
-                        val = (MODE == MODE_POLY) ? __fadd_rn(__fmul_rn(alpha, ev), __fmul_rn(beta, val))
-                                                  : __fadd_rn(__fmul_rn(alpha, ev), val);
+                    if (MODE == MODE_POLY) {
+                        const uint16_t ebits =
+                            *reinterpret_cast<const uint16_t*>(brow + (((j >> 3) ^ sw) << 4) + (j & 7) * 2);
+                        const float ev = __uint_as_float(static_cast<uint32_t>(ebits) << 16);
+                        val = __fadd_rn(__fmul_rn(alpha, ev), __fmul_rn(beta, val));
                     }
-                    const uint16_t b = to_bf16(val);
-                    if (MODE == MODE_UPDATE) {
-                        drow[col] = b;
-                    } else {
-                        if (col >= row) drow[col] = b;
-                        if (col > row) D[static_cast<int64_t>(col) * g.ld + row] = b;
-                    }
+                    const uint16_t bv = to_bf16(val);
+                    drow[col] = bv;
+                    if (col > row) D[static_cast<int64_t>(col) * g.ld + row] = bv;
                 }
             }
         }
+        if (lane == 0) {
+            bulk_commit();
+            bulk_wait_read<RING - AHEAD>();
+        }
+        __syncwarp();
+        if (k + AHEAD < nblocks) issue(k + AHEAD);
     }
+    eb.seq = s0 + static_cast<uint32_t>(nblocks);
     return true;
 }
 
@@ -427,14 +517,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tiles = smem;
-    uint32_t* xpose_all = reinterpret_cast<uint32_t*>(smem + STAGES * STAGE_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + XPOSE_BYTES);
+    uint8_t* ebufs = smem + STAGES * STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ebufs + EBUFS_BYTES);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + STAGES;
     uint64_t* tfull_bar = bars + 2 * STAGES;
     uint64_t* tempty_bar = bars + 2 * STAGES + 2;
     uint64_t* drain_bar = bars + 2 * STAGES + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    uint64_t* ebar = bars + 2 * STAGES + 5;  // NSLOT per epilogue warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ebar + NSLOT * EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -450,6 +541,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             mbar_init(smem_u32(&tempty_bar[a]), EPI_WARPS);
         }
         mbar_init(smem_u32(drain_bar), 1);
+        for (int i = 0; i < NSLOT * EPI_WARPS; ++i) mbar_init(smem_u32(&ebar[i]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -457,6 +549,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         for (int gi = 0; gi < p.num_groups; ++gi) {
             tma_prefetch_desc(&p.g[gi].tm_a);
             tma_prefetch_desc(&p.g[gi].tm_b);
+            if (MODE != MODE_SYRK) tma_prefetch_desc(&p.g[gi].tm_e);
+            tma_prefetch_desc(&p.g[gi].tm_d);
+            if (MODE != MODE_UPDATE) tma_prefetch_desc(&p.g[gi].tm_m);
         }
     }
     if (warp == 1) {
@@ -505,8 +600,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         }
         // drain: every issued copy must land before the CTA may exit
         for (int s = 0; s < STAGES; ++s) {
-            if (last_parity[s] >= 0)
-                wait_bounded(smem_u32(&full_bar[s]), static_cast<uint32_t>(last_parity[s]), abort_flag, p.status);
+            if (last_parity[s] >= 0) wait_drain(smem_u32(&full_bar[s]), static_cast<uint32_t>(last_parity[s]));
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
@@ -550,25 +644,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         }
         // drain: all issued MMAs complete before TMEM is released
         tc_commit(smem_u32(drain_bar));
-        wait_bounded(smem_u32(drain_bar), 0, abort_flag, p.status);
+        wait_drain(smem_u32(drain_bar), 0);
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
         const int quarter = warp & 3;        // TMEM lanes 32*quarter .. +31
         const int half = (warp - 2) >> 2;    // column half when two warps share a quarter
-        uint32_t* xpose = xpose_all + (warp - 2) * XPOSE_WORDS;
+        const int ew = warp - 2;
+        EpiBufs eb;
+        for (int b = 0; b < NSLOT; ++b) {
+            eb.ptr[b] = ebufs + (NSLOT * ew + b) * EBUF_BYTES;
+            eb.buf[b] = smem_u32(eb.ptr[b]);
+            eb.bar[b] = smem_u32(&ebar[NSLOT * ew + b]);
+        }
+        eb.phase = 0;
+        eb.pending = 0;
+        eb.seq = 0;
         int local = 0;
         for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
             const Tile tile = decode_tile<MODE>(p, t);
             const GroupParams& g = p.g[tile.group];
             const int acc = local & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
-            if (!epilogue_tile<MODE>(p, g, tile, tmem_base + static_cast<uint32_t>(acc * BN), quarter, half, lane, xpose,
-                                     smem_u32(&tfull_bar[acc]), acc_phase, abort_flag))
+            if (!epilogue_tile<MODE>(p, g, tile, tmem_base + static_cast<uint32_t>(acc * BN), quarter, half, lane,
+                                     smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, eb))
                 break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
         }
+        // drain: addend loads still in flight land, and the output stores
+        // complete, before the CTA exits
+        for (int b = 0; b < NSLOT; ++b)
+            if (eb.pending & (1u << b)) wait_drain(eb.bar[b], (eb.phase >> b) & 1u);
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -604,7 +713,8 @@ EncodeTiledFn encode_fn() {
 // 3-D bf16 tensor map over [count][rows][inner] with row stride ld elements
 // and matrix stride `mat_stride` bytes.
 bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t count, int64_t ld,
-              int64_t mat_stride, uint32_t box_inner, uint32_t box_rows) {
+              int64_t mat_stride, uint32_t box_inner, uint32_t box_rows,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
@@ -613,7 +723,7 @@ bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, i
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -646,6 +756,8 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, f
         if (MODE == MODE_SYRK) {
             ok &= make_map(&g.tm_a, X, G.np, G.mp, G.count, G.ldx, G.x_stride, BK, BM);
             ok &= make_map(&g.tm_b, X, G.np, G.mp, G.count, G.ldx, G.x_stride, BK, BN);
+            ok &= make_map(&g.tm_d, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+            ok &= make_map(&g.tm_m, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
             g.E = nullptr;
             g.D = G.A;
             g.ld = G.lda;
@@ -656,6 +768,9 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, f
         } else if (MODE == MODE_POLY) {
             ok &= make_map(&g.tm_a, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, BK, BM);
             ok &= make_map(&g.tm_b, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, BK, BN);
+            ok &= make_map(&g.tm_e, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+            ok &= make_map(&g.tm_d, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+            ok &= make_map(&g.tm_m, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
             g.E = G.A;
             g.D = G.B;
             g.ld = G.lda;
@@ -666,6 +781,9 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, f
         } else {
             ok &= make_map(&g.tm_a, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, BK, BM);
             ok &= make_map(&g.tm_b, X, G.np, G.mp, G.count, G.ldx, G.x_stride, 64, BK);
+            ok &= make_map(&g.tm_e, X, G.np, G.mp, G.count, G.ldx, G.x_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+            ok &= make_map(&g.tm_d, G.X[cur ^ 1], G.np, G.mp, G.count, G.ldx, G.x_stride, 32, 32,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
             g.E = X;
             g.D = G.X[cur ^ 1];
             g.ld = G.ldx;
