@@ -110,6 +110,24 @@ def aggregate_tflops(flops_per_step: int, steps: int, world: int, ms_total_max: 
     return flops_per_step * steps * world / (ms_total_max / 1e3) / 1e12
 
 
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture
+    (profiles/ncu_traffic.json), scaled to the full workload; None when the
+    kernel source changed since the capture or the workload differs."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f)
+        with open(os.path.join(ROOT, rec["source_file"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if sha != rec["source_sha256"] or workload != rec["workload"]:
+            return None
+        b = rec["captured_bytes"][kernel]
+        return (b["read"] + b["write"]) * rec["scale_to_full_launch"]
+    except Exception:
+        return None
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -394,7 +412,8 @@ def run_ours(args, rank, world, local_rank):
                     "unit": "TFLOP/s", "frac": achieved / peak,
                     "peak_kind": f"bf16 sustained, {peaks['source']}",
                     "algorithmic_per_launch": per_launch, "ms_per_launch": ms_launch,
-                    "traffic": None}
+                    "traffic": None if args.subset else ncu_traffic(dominant, w.name),
+                    "traffic_unit": "bytes per launch (DRAM read + write, ncu)"}
     else:
         per_launch = ew_bytes[dominant] / d["launches_per_step"]
         ms_launch = d["ms_per_step"] / d["launches_per_step"]
