@@ -604,7 +604,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
-        constexpr uint32_t idesc = instr_desc(BM, BN, MODE == MODE_UPDATE);
         int stage = 0;
         uint32_t phase = 0;
         int local = 0;
@@ -617,7 +616,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
             if (!wait_bounded(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, abort_flag, p.status)) break;
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            // Columns of the tile the MMAs compute, [n_lo, n_hi): an odd row
+            // tile on the diagonal of SYRK/POLY needs only its right half (the
+            // left half lies below the diagonal), and the last column tile of
+            // a ragged matrix only up to the next multiple of 16 past N.
+            int n_lo = 0, n_hi = BN;
+            if (MODE != MODE_UPDATE && (tile.ti & 1) && tile.tj == (tile.ti >> 1)) n_lo = BN / 2;
+            const int rem = g.N - tile.tj * BN;
+            if (rem < BN) n_hi = (rem + 15) & ~15;
+            const uint32_t idesc = instr_desc(BM, n_hi - n_lo, MODE == MODE_UPDATE);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN + n_lo);
+            const uint32_t b_off = static_cast<uint32_t>(n_lo) * 128;  // K-major B rows are 128 bytes
             for (int kb = 0; kb < nk; ++kb) {
                 if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.status)) {
                     ok = false;
@@ -630,7 +639,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
                 for (int k = 0; k < BK / 16; ++k) {
                     const uint64_t adesc = smem_desc(sa + k * 32, 16, 1024);
                     const uint64_t bdesc = (MODE == MODE_UPDATE) ? smem_desc(sb + k * 16 * 128, 64 * BK * 2, 1024)
-                                                                 : smem_desc(sb + k * 32, 16, 1024);
+                                                                 : smem_desc(sb + b_off + k * 32, 16, 1024);
                     tc_mma(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
                 }
                 tc_commit(smem_u32(&empty_bar[stage]));
