@@ -79,7 +79,7 @@ def run_ns(shape, count, steps=5, coeffs=oracle.QUINTIC, seed=0, kind="gaussian"
 
 @pytest.mark.parametrize("coeffs,what", [((1.0, 0.0, 0.0), "identity"), ((0.0, 1.0, 0.0), "AX"),
                                          ((0.0, 0.0, 1.0), "AAX")])
-@pytest.mark.parametrize("shape", [(64, 64), (128, 256), (200, 328), (256, 512)])
+@pytest.mark.parametrize("shape", [(64, 64), (128, 256), (200, 328), (256, 512), (512, 900)])
 def test_ns_single_stage_isolation(lib, shape, coeffs, what):
     """One step with one coefficient set isolates one product:
     (1,0,0) -> X;  (0,1,0) -> (X X^T) X;  (0,0,1) -> (X X^T)^2 X."""
@@ -92,8 +92,11 @@ def test_ns_single_stage_isolation(lib, shape, coeffs, what):
             assert rel_fro(got[i], ref) < NS_TOL, what
 
 
+# m' a multiple of 256 runs on CTA pairs (256x256 pair tiles), other m' on
+# single CTAs; both kinds, ragged edges included, are covered here.
 @pytest.mark.parametrize("shape", [(1, 1), (7, 13), (8, 8), (64, 64), (128, 256), (129, 257),
-                                   (200, 328), (256, 512), (300, 1000), (384, 384)])
+                                   (200, 328), (256, 512), (300, 1000), (384, 384),
+                                   (512, 512), (512, 900), (768, 800)])
 def test_ns_parity(lib, shape):
     count = 3 if shape[0] * shape[1] < 200_000 else 1
     X, got = run_ns(shape, count, seed=11)
@@ -145,7 +148,8 @@ def check_step(W0, G0, M0, W1, M1, hp):
     return oW
 
 
-SHAPES = [(256, 512), (512, 256), (7, 13), (13, 7), (1, 1), (130, 70), (64, 1024), (300, 300)]
+SHAPES = [(256, 512), (512, 256), (7, 13), (13, 7), (1, 1), (130, 70), (64, 1024), (300, 300),
+          (512, 900), (900, 512)]
 
 
 @pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
