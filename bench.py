@@ -40,7 +40,7 @@ METRIC = "Muon optimizer-step ms & NS TFLOP/s (frac of BF16 peak); AdamW HBM GB/
 UNIT = "TFLOP/s"
 ADAMW_BYTES_PER_PARAM = 28  # read p, g, m, v (16 B), write p, m, v (12 B)
 KINDS = ("momentum_norm", "norm_finalize", "normalize_cast", "ns_syrk", "ns_poly", "ns_update",
-         "final_update", "adamw")
+         "final_update", "adamw", "grad_guard")
 
 
 def parse():
@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-guard", action="store_true")
     ap.add_argument("--subset", type=int, default=0,
                     help="profiling only: keep the first N matrices of the workload")
     return ap.parse_args()
@@ -437,6 +438,32 @@ def run_ours(args, rank, world, local_rank):
                   "frac_of_peak_algorithmic": step_flops / (ns_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
                   "frac_of_peak_dense_equivalent": dense_flops / (ns_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"]}
 
+    # ---- the step with the call-wide gradient guard on (skip on non-finite,
+    # clip by the global norm): an extra read of every gradient ----
+    guard = None
+    if not args.no_guard:
+        ghp = m.MuonHparams(**dict(workloads.MUON_HPARAMS, skip_nonfinite=True, max_grad_norm=1e9))
+        for _ in range(2):
+            batch.step(ghp, stream)
+        torch.cuda.synchronize()
+        m.muon_set_timing(True)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        n_guard = max(3, min(args.steps, 10))
+        for _ in range(n_guard):
+            batch.step(ghp, stream)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        gk = m.muon_timing_read()["grad_guard"]
+        m.muon_set_timing(False)
+        if m.muon_query_status(batch.workspace) != 0:
+            raise RuntimeError("device status set in the guarded run")
+        g_bytes = sum(s.rows * s.cols * (2 if s.g_dtype.itemsize == 2 else 4) for s in w.matrices)
+        guard_ms = gk[0] / n_guard
+        guard = {"ms_per_step": g0.elapsed_time(g1) / n_guard, "guard_kernels_ms_per_step": guard_ms,
+                 "guard_gbs": g_bytes / (guard_ms / 1e3) / 1e9, "guard_bytes_per_step": g_bytes,
+                 "settings": "skip_nonfinite=1, max_grad_norm=1e9"}
+
     # ---- end to end through the public API, host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -495,7 +522,7 @@ def run_ours(args, rank, world, local_rank):
                            "l2": "inputs > 12 GB exceed the 129 MB L2; no flush needed",
                            "parallelism": "replicas" if world > 1 else "single"},
                 "roofline": roofline, "ns": ns_summary, "stages": stages, "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": launches, "clocks": clk, "adamw": adamw}
+                "e2e": e2e, "gpu_launches": launches, "clocks": clk, "adamw": adamw, "guarded_step": guard}
         print(json.dumps(line), flush=True)
 
 

@@ -35,7 +35,9 @@ typedef enum {
     MUON_ERR_WORKSPACE_TOO_SMALL = 4,  /* a single matrix needs more          */
     MUON_ERR_CUDA = 5,                 /* a CUDA runtime call failed          */
     MUON_ERR_TIMEOUT = 6,              /* a kernel gave up on a bounded wait  */
-    MUON_ERR_NO_DEVICE = 7             /* no sm_103 device is current         */
+    MUON_ERR_NO_DEVICE = 7,            /* no sm_103 device is current         */
+    MUON_STEP_SKIPPED = 8              /* (device status) the non-finite guard
+                                          skipped the step; nothing changed   */
 } muon_status_t;
 
 typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype_t;
@@ -58,7 +60,8 @@ typedef struct {
 /* Hyper-parameters of one Muon step, all applied as fp32 values.
  * Defaults of the reference configuration: lr 0.02, weight_decay 0.1,
  * momentum 0.95, nesterov 1, ns_steps 5, (ns_a, ns_b, ns_c) =
- * (3.4445, -4.7750, 2.0315), norm_eps 1e-7, rms_scale 0.2. */
+ * (3.4445, -4.7750, 2.0315), norm_eps 1e-7, rms_scale 0.2, scale_mode 0,
+ * skip_nonfinite 0, max_grad_norm 0, ns_coeffs NULL. */
 typedef struct {
     float lr;
     float weight_decay;
@@ -67,7 +70,26 @@ typedef struct {
     int32_t ns_steps;  /* Newton-Schulz steps, 0..100                        */
     float ns_a, ns_b, ns_c;
     float norm_eps;    /* added to the Frobenius norm, >= 0                  */
-    float rms_scale;   /* update = rms_scale * sqrt(max(rows, cols)) * O     */
+    float rms_scale;   /* scale_mode 0: update = rms_scale sqrt(max(m,n)) O  */
+    /* Update scale ([K2] section 3): 0 = rms_scale * sqrt(max(rows, cols)),
+     * matching AdamW's update RMS (section 3.1); 1 = max(1, sqrt(rows/cols))
+     * = max(1, sqrt(d_out/d_in)), the muP-style adjustment (section 3.2).  */
+    int32_t scale_mode;
+    /* [OPT] section 5.4, the "Inf guard": 1 = if any gradient element of
+     * the call is NaN or +-inf, change nothing (every W and M keeps its old
+     * value) and record MUON_STEP_SKIPPED in the workspace status.          */
+    int32_t skip_nonfinite;
+    /* [OPT] section 5.4, gradient clipping as a safety net: > 0 = scale all
+     * gradients of the call by clip = min(1, max_grad_norm / (||G||_global
+     * + 1e-6)) (fp64, rounded to fp32; ||G||_global over every element of
+     * every matrix of the call) before the momentum update.  <= 0: off.     */
+    float max_grad_norm;
+    int32_t reserved0; /* must be 0                                          */
+    /* NULL: (ns_a, ns_b, ns_c) at every NS step.  Otherwise host memory of
+     * 3 * ns_steps floats, step s using (a, b, c) = ns_coeffs[3s..3s+2]
+     * (e.g. the page's cubic (1.5, -0.5, 0), [OPT] section 4.2, or a
+     * per-step schedule); read before the call returns.                    */
+    const float* ns_coeffs;
 } muon_hparams_t;
 
 /* One row of the execution plan (see muon_plan). */
@@ -161,14 +183,18 @@ muon_status_t muon_step_batched_noalloc(const muon_matrix_t* mats, int64_t count
 /* Newton-Schulz alone on a batch of `count` wide bf16 matrices (device,
  * [count][mp][np] row-major, bf16 bit patterns, mp <= np), writing the
  * result to X_out (same layout; may not alias X_in):
- *   ns_steps times: A = X X^T; B = b A + c A A; X = a X + B X.
- * workspace: device, >= count * muon_workspace_bytes_per_matrix(mp, np),
- * 256-byte aligned.  X_in and X_out must be 16-byte aligned. */
+ *   for s < ns_steps: A = X X^T; B = b A + c A A; X = a X + B X
+ * ([OPT] section 4.2) with (a, b, c) = coeffs[0..2] at every step when
+ * ncoeff_sets == 1, or coeffs[3s..3s+2] when ncoeff_sets == ns_steps
+ * (host memory, read before the call returns).
+ * workspace: device, >= muon_workspace_bytes_per_matrix(mp, np) (larger
+ * batches run in several passes), 256-byte aligned.  X_in and X_out must
+ * be 2-byte aligned. */
 muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out,
                                  int64_t count, int64_t mp, int64_t np,
-                                 int32_t ns_steps, float a, float b, float c,
-                                 void* workspace, size_t ws_bytes,
-                                 void* stream);
+                                 int32_t ns_steps, const float* coeffs,
+                                 int32_t ncoeff_sets, void* workspace,
+                                 size_t ws_bytes, void* stream);
 
 /* AdamW on flat fp32 device buffers of n elements, in place on p, m, v
  * ([OPT] sections 2.3 and 3.1), step >= 1:
@@ -183,7 +209,8 @@ muon_status_t adamw_step(float* p, const float* g, float* m, float* v,
                          void* stream);
 
 /* Synchronises `stream`, reads and clears the status word a step left in
- * `workspace`; returns MUON_OK or the recorded error (MUON_ERR_TIMEOUT). */
+ * `workspace`; returns MUON_OK or what was recorded (MUON_ERR_TIMEOUT,
+ * MUON_STEP_SKIPPED). */
 muon_status_t muon_query_status(void* workspace, void* stream);
 
 /* ---- Instrumentation (no counterpart on the pages) --------------------- */
@@ -198,7 +225,8 @@ typedef enum {
     MUON_KERNEL_NS_UPDATE = 5,      /* X = a X + B X                        */
     MUON_KERNEL_FINAL_UPDATE = 6,   /* W -= lr (wd W + scale O)             */
     MUON_KERNEL_ADAMW = 7,          /* AdamW                                */
-    MUON_KERNEL_COUNT = 8
+    MUON_KERNEL_GRAD_GUARD = 8,     /* global gradient norm / non-finite    */
+    MUON_KERNEL_COUNT = 9
 } muon_kernel_kind_t;
 
 /* Process-wide count of kernels this library has launched (all kinds). */

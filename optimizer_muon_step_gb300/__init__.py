@@ -33,7 +33,8 @@ _lib = None
 MUON_F32, MUON_BF16 = 0, 1
 STATUS = {0: "MUON_OK", 1: "MUON_ERR_INVALID_ARG", 2: "MUON_ERR_UNSUPPORTED_DTYPE",
           3: "MUON_ERR_MISALIGNED", 4: "MUON_ERR_WORKSPACE_TOO_SMALL", 5: "MUON_ERR_CUDA",
-          6: "MUON_ERR_TIMEOUT", 7: "MUON_ERR_NO_DEVICE"}
+          6: "MUON_ERR_TIMEOUT", 7: "MUON_ERR_NO_DEVICE", 8: "MUON_STEP_SKIPPED"}
+MUON_STEP_SKIPPED = 8
 
 # Every symbol include/muon_step.h declares.
 EXPORTS = ("muon_workspace_bytes_per_matrix", "muon_workspace_size", "muon_plan",
@@ -41,7 +42,7 @@ EXPORTS = ("muon_workspace_bytes_per_matrix", "muon_workspace_size", "muon_plan"
            "muon_status_string", "muon_version", "muon_launch_count", "muon_set_timing",
            "muon_timing_read", "muon_kernel_name", "muon_step_batched_noalloc")
 KERNEL_KINDS = ("momentum_norm", "norm_finalize", "normalize_cast", "ns_syrk", "ns_poly",
-                "ns_update", "final_update", "adamw")
+                "ns_update", "final_update", "adamw", "grad_guard")
 
 
 class MuonError(RuntimeError):
@@ -61,7 +62,10 @@ class _MuonHparamsC(ctypes.Structure):
                 ("momentum", ctypes.c_float), ("nesterov", ctypes.c_int32),
                 ("ns_steps", ctypes.c_int32), ("ns_a", ctypes.c_float),
                 ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float),
-                ("norm_eps", ctypes.c_float), ("rms_scale", ctypes.c_float)]
+                ("norm_eps", ctypes.c_float), ("rms_scale", ctypes.c_float),
+                ("scale_mode", ctypes.c_int32), ("skip_nonfinite", ctypes.c_int32),
+                ("max_grad_norm", ctypes.c_float), ("reserved0", ctypes.c_int32),
+                ("ns_coeffs", ctypes.c_void_p)]
 
 
 class _AdamwHparamsC(ctypes.Structure):
@@ -93,11 +97,31 @@ class MuonHparams:
     ns_c: float = 2.0315
     norm_eps: float = 1e-7
     rms_scale: float = 0.2
+    scale_mode: int = 0            # 0: rms_scale*sqrt(max(m,n)); 1: max(1, sqrt(rows/cols))
+    skip_nonfinite: bool = False   # skip the whole call when any gradient is non-finite
+    max_grad_norm: float = 0.0     # > 0: clip all gradients of the call by their global norm
+    ns_coeffs: object = None       # None, or ns_steps (a, b, c) triples
 
     def _c(self):
-        return _MuonHparamsC(self.lr, self.weight_decay, self.momentum, int(bool(self.nesterov)),
-                             int(self.ns_steps), self.ns_a, self.ns_b, self.ns_c, self.norm_eps,
-                             self.rms_scale)
+        h = _MuonHparamsC(self.lr, self.weight_decay, self.momentum, int(bool(self.nesterov)),
+                          int(self.ns_steps), self.ns_a, self.ns_b, self.ns_c, self.norm_eps,
+                          self.rms_scale, int(self.scale_mode), int(bool(self.skip_nonfinite)),
+                          self.max_grad_norm, 0, None)
+        if self.ns_coeffs is not None:
+            table = _coeff_array(self.ns_coeffs, self.ns_steps)
+            h.ns_coeffs = ctypes.cast(table, ctypes.c_void_p)
+            h._keep = table  # alive as long as the struct
+        return h
+
+
+def _coeff_array(coeffs, steps):
+    """(ctypes float array, count of triples) from one triple or a list of them."""
+    flat = [float(x) for x in np.asarray(coeffs, dtype=np.float64).reshape(-1)]
+    if len(flat) % 3:
+        raise ValueError("NS coefficients come in (a, b, c) triples")
+    if len(flat) // 3 not in (1, max(int(steps), 1)) and steps:
+        raise ValueError("give one (a, b, c) triple or one per NS step")
+    return (ctypes.c_float * len(flat))(*flat)
 
 
 @dataclass
@@ -133,8 +157,7 @@ def load_library(path: str = LIB_PATH):
         lib.muon_step_batched.restype = ctypes.c_int
         lib.muon_step_batched_noalloc.argtypes = [P, i64, P, P]
         lib.muon_step_batched_noalloc.restype = ctypes.c_int
-        lib.muon_newton_schulz.argtypes = [P, P, i64, i64, i64, i32, ctypes.c_float, ctypes.c_float,
-                                           ctypes.c_float, P, ctypes.c_size_t, P]
+        lib.muon_newton_schulz.argtypes = [P, P, i64, i64, i64, i32, P, i32, P, ctypes.c_size_t, P]
         lib.muon_newton_schulz.restype = ctypes.c_int
         lib.adamw_step.argtypes = [P, P, P, P, i64, P, i64, P]
         lib.adamw_step.restype = ctypes.c_int
@@ -283,7 +306,9 @@ def muon_step_batched_noalloc(W, G, M, hp: MuonHparams = MuonHparams(), stream=N
 
 def muon_newton_schulz(X, steps: int = 5, coeffs=(3.4445, -4.7750, 2.0315), out=None,
                        workspace=None, stream=None):
-    """Newton-Schulz on a bf16 CUDA tensor [count, m', n'] (or [m', n'])."""
+    """Newton-Schulz on a bf16 CUDA tensor [count, m', n'] (or [m', n']).
+
+    coeffs: one (a, b, c) triple for every step, or `steps` triples."""
     import torch
     _dev_tensor(X, "X", (torch.bfloat16,))
     squeeze = X.dim() == 2
@@ -298,11 +323,11 @@ def muon_newton_schulz(X, steps: int = 5, coeffs=(3.4445, -4.7750, 2.0315), out=
     lib = load_library()
     if workspace is None:
         workspace = allocate_workspace(count * muon_workspace_bytes_per_matrix(mp, np_), X.device)
-    a, b, c = coeffs
+    table = _coeff_array(coeffs, steps)
     _check(lib.muon_newton_schulz(ctypes.c_void_p(X3.data_ptr()), ctypes.c_void_p(out3.data_ptr()),
-                                  count, mp, np_, int(steps), float(a), float(b), float(c),
-                                  ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                                  _stream(stream)), "muon_newton_schulz")
+                                  count, mp, np_, int(steps), ctypes.cast(table, ctypes.c_void_p),
+                                  len(table) // 3, ctypes.c_void_p(workspace.data_ptr()),
+                                  workspace.numel(), _stream(stream)), "muon_newton_schulz")
     return out3[0] if squeeze else out3
 
 
@@ -321,7 +346,8 @@ def adamw_step(p, g, m, v, hp: AdamwHparams = AdamwHparams(), step: int = 1, str
 
 
 def muon_query_status(workspace, stream=None) -> int:
-    """Synchronises the stream and returns (and clears) the device status."""
+    """Synchronises the stream and returns (and clears) the device status:
+    0, MUON_ERR_TIMEOUT (6) or MUON_STEP_SKIPPED (8)."""
     return int(load_library().muon_query_status(ctypes.c_void_p(workspace.data_ptr()), _stream(stream)))
 
 

@@ -4,7 +4,7 @@
 //
 // Workspace layout of one chunk of n matrices (n * 8192 record bytes plus
 // the X / Gram buffers of muon_workspace_bytes_per_matrix):
-//   [0, 256)                 header: int32 status word at offset 0
+//   [0, 256)                 WsHeader: status word, gradient-guard results
 //   [256, ...)               MatDesc[n]
 //   [.., +n*4096)            norm partial sums, 1024 floats per matrix
 //   [n*8192, ...)            per shape group of c matrices:
@@ -23,7 +23,7 @@ using namespace muon;
 
 namespace {
 
-constexpr int32_t kVersion = 100;  // 0.1.0
+constexpr int32_t kVersion = 200;  // 0.2.0
 
 inline int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
 
@@ -70,7 +70,35 @@ muon_status_t check_hparams(const muon_hparams_t* hp) {
     if (hp->momentum < 0.f || hp->momentum > 1.f || hp->norm_eps < 0.f) return MUON_ERR_INVALID_ARG;
     if (hp->ns_steps < 0 || hp->ns_steps > 100) return MUON_ERR_INVALID_ARG;
     if (hp->nesterov != 0 && hp->nesterov != 1) return MUON_ERR_INVALID_ARG;
+    if (hp->scale_mode != 0 && hp->scale_mode != 1) return MUON_ERR_INVALID_ARG;
+    if (hp->skip_nonfinite != 0 && hp->skip_nonfinite != 1) return MUON_ERR_INVALID_ARG;
+    if (!finite(hp->max_grad_norm) || hp->reserved0 != 0) return MUON_ERR_INVALID_ARG;
+    if (hp->ns_coeffs)
+        for (int i = 0; i < 3 * hp->ns_steps; ++i)
+            if (!finite(hp->ns_coeffs[i])) return MUON_ERR_INVALID_ARG;
     return MUON_OK;
+}
+
+// Per-step NS coefficients, 3 * steps floats.
+std::vector<float> coeff_table(const muon_hparams_t* hp) {
+    std::vector<float> t(3 * static_cast<size_t>(hp->ns_steps));
+    for (int s = 0; s < hp->ns_steps; ++s) {
+        t[3 * s] = hp->ns_coeffs ? hp->ns_coeffs[3 * s] : hp->ns_a;
+        t[3 * s + 1] = hp->ns_coeffs ? hp->ns_coeffs[3 * s + 1] : hp->ns_b;
+        t[3 * s + 2] = hp->ns_coeffs ? hp->ns_coeffs[3 * s + 2] : hp->ns_c;
+    }
+    return t;
+}
+
+// The update's scale factor (fp64, rounded to fp32): mode 0 matches AdamW's
+// update RMS, rms_scale * sqrt(max(rows, cols)); mode 1 is the muP-style
+// max(1, sqrt(d_out / d_in)) with (d_out, d_in) = (rows, cols).
+float update_scale(const muon_hparams_t* hp, int64_t rows, int64_t cols) {
+    if (hp->scale_mode == 1) {
+        const double r = sqrt(static_cast<double>(rows) / static_cast<double>(cols));
+        return static_cast<float>(r > 1.0 ? r : 1.0);
+    }
+    return static_cast<float>(static_cast<double>(hp->rms_scale) * sqrt(static_cast<double>(std::max(rows, cols))));
 }
 
 muon_status_t check_shapes(const muon_matrix_t* mats, int64_t count) {
@@ -205,6 +233,7 @@ const char* muon_status_string(muon_status_t s) {
         case MUON_ERR_CUDA: return "CUDA runtime error";
         case MUON_ERR_TIMEOUT: return "kernel timed out on a bounded wait";
         case MUON_ERR_NO_DEVICE: return "no sm_103 device is current";
+        case MUON_STEP_SKIPPED: return "step skipped by the non-finite gradient guard";
     }
     return "unknown status";
 }
@@ -271,26 +300,31 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    int* status = reinterpret_cast<int*>(ws);
-    s = from_cuda(cudaMemsetAsync(status, 0, sizeof(int), st));
+    WsHeader* header = reinterpret_cast<WsHeader*>(ws);
+    s = from_cuda(cudaMemsetAsync(header, 0, sizeof(WsHeader), st));
     if (s != MUON_OK) return s;
 
-    const MomentumScalars ms{hp->momentum, 1.0f - hp->momentum, hp->nesterov};
-    const UpdateScalars us{hp->lr, hp->weight_decay};
+    const bool clip_on = hp->max_grad_norm > 0.f;
+    const bool guard_on = clip_on || hp->skip_nonfinite;
+    const MomentumScalars ms{hp->momentum, 1.0f - hp->momentum, hp->nesterov, clip_on ? 1 : 0,
+                             guard_on ? header : nullptr};
+    const UpdateScalars us{hp->lr, hp->weight_decay, guard_on ? header : nullptr};
+    const std::vector<float> coeffs = coeff_table(hp);
     ChunkLayout L;
     std::vector<MatDesc> descs;
-    size_t b = 0;
-    while (b < plan.size()) {
-        size_t e = b;
-        while (e < plan.size() && plan[e].chunk == plan[b].chunk) ++e;
+    MatDesc* d_descs = reinterpret_cast<MatDesc*>(ws + kHeaderBytes);
+    int max_tiles = 1;
+    int64_t max_rows = 1, max_cols = 1;
+
+    // Fills `descs` and the layout for plan rows [b, e) and uploads them.
+    auto prepare_chunk = [&](size_t b, size_t e) -> muon_status_t {
         const int n = static_cast<int>(e - b);
         layout_groups(plan, b, e, ws, L);
-        MatDesc* d_descs = reinterpret_cast<MatDesc*>(ws + kHeaderBytes);
         float* d_partials = reinterpret_cast<float*>(
             ws + kHeaderBytes + round_up(static_cast<int64_t>(n) * static_cast<int64_t>(sizeof(MatDesc)), 256));
         descs.assign(n, MatDesc{});
-        int max_tiles = 1;
-        int64_t max_rows = 1, max_cols = 1;
+        max_tiles = 1;
+        max_rows = max_cols = 1;
         for (int k = 0; k < n; ++k) {
             const PlanRow& row = plan[b + k];
             const muon_matrix_t& m = mats[row.idx];
@@ -318,35 +352,73 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
             d.vec = ((reinterpret_cast<uintptr_t>(m.W) | reinterpret_cast<uintptr_t>(m.G) |
                       reinterpret_cast<uintptr_t>(m.M)) & 15u) == 0 ? 1 : 0;
             d.scale = 0.f;
-            d.update_scale = static_cast<float>(static_cast<double>(hp->rms_scale) * sqrt(static_cast<double>(row.np)));
+            d.update_scale = update_scale(hp, m.rows, m.cols);
             max_tiles = std::max(max_tiles, d.ntiles);
             max_rows = std::max(max_rows, m.rows);
             max_cols = std::max(max_cols, m.cols);
         }
-        s = from_cuda(cudaMemcpyAsync(d_descs, descs.data(), sizeof(MatDesc) * n, cudaMemcpyHostToDevice, st));
+        return from_cuda(cudaMemcpyAsync(d_descs, descs.data(), sizeof(MatDesc) * n, cudaMemcpyHostToDevice, st));
+    };
+
+    // chunk boundaries
+    std::vector<std::pair<size_t, size_t>> chunks;
+    for (size_t b = 0; b < plan.size();) {
+        size_t e = b;
+        while (e < plan.size() && plan[e].chunk == plan[b].chunk) ++e;
+        chunks.emplace_back(b, e);
+        b = e;
+    }
+
+    // Gradient guard over every matrix of the call, before any state changes.
+    if (guard_on) {
+        for (const auto& c : chunks) {
+            s = prepare_chunk(c.first, c.second);
+            if (s != MUON_OK) return s;
+            const int n = static_cast<int>(c.second - c.first);
+            s = from_cuda(launch_grad_stats(d_descs, n, max_tiles, header, st));
+            if (s != MUON_OK) return s;
+            s = from_cuda(launch_grad_stats_reduce(d_descs, n, header, st));
+            if (s != MUON_OK) return s;
+        }
+        s = from_cuda(launch_grad_decide(header, hp->max_grad_norm, hp->skip_nonfinite, st));
         if (s != MUON_OK) return s;
+    }
+
+    for (size_t ci = 0; ci < chunks.size(); ++ci) {
+        const size_t b = chunks[ci].first, e = chunks[ci].second;
+        const int n = static_cast<int>(e - b);
+        if (!(guard_on && chunks.size() == 1)) {  // a single chunk is still in place from the guard
+            s = prepare_chunk(b, e);
+            if (s != MUON_OK) return s;
+        }
         s = from_cuda(launch_momentum_norm(d_descs, n, max_tiles, ms, st));
         if (s != MUON_OK) return s;
         s = from_cuda(launch_norm_finalize(d_descs, n, hp->norm_eps, st));
         if (s != MUON_OK) return s;
         s = from_cuda(launch_normalize_cast(d_descs, n, max_rows, max_cols, ms, st));
         if (s != MUON_OK) return s;
-        s = from_cuda(ns_run(L.groups.data(), static_cast<int>(L.groups.size()), hp->ns_steps, hp->ns_a, hp->ns_b,
-                             hp->ns_c, status, num_sms, st));
+        s = from_cuda(ns_run(L.groups.data(), static_cast<int>(L.groups.size()), hp->ns_steps, coeffs.data(),
+                             &header->status, num_sms, st));
         if (s != MUON_OK) return s;
         s = from_cuda(launch_final_update(d_descs, n, max_rows, max_cols, us, st));
         if (s != MUON_OK) return s;
-        b = e;
     }
     return MUON_OK;
 }
 
 muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t count, int64_t mp, int64_t np,
-                                 int32_t ns_steps, float a, float b, float c, void* workspace, size_t ws_bytes,
-                                 void* stream) {
+                                 int32_t ns_steps, const float* coeff_in, int32_t ncoeff_sets, void* workspace,
+                                 size_t ws_bytes, void* stream) {
     if (count < 0 || mp <= 0 || np <= 0 || mp > np || ns_steps < 0 || ns_steps > 100) return MUON_ERR_INVALID_ARG;
     if (np > (int64_t(1) << 30)) return MUON_ERR_INVALID_ARG;
-    if (!finite(a) || !finite(b) || !finite(c)) return MUON_ERR_INVALID_ARG;
+    if (ns_steps > 0 && (!coeff_in || (ncoeff_sets != 1 && ncoeff_sets != ns_steps))) return MUON_ERR_INVALID_ARG;
+    std::vector<float> coeffs(3 * static_cast<size_t>(ns_steps));
+    for (int st = 0; st < ns_steps; ++st)
+        for (int j = 0; j < 3; ++j) {
+            const float v = coeff_in[(ncoeff_sets == 1 ? 0 : 3 * st) + j];
+            if (!finite(v)) return MUON_ERR_INVALID_ARG;
+            coeffs[3 * st + j] = v;
+        }
     if (count == 0) return MUON_OK;
     if (!X_in || !X_out || !workspace) return MUON_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(X_in) | reinterpret_cast<uintptr_t>(X_out)) & 1u) return MUON_ERR_MISALIGNED;
@@ -359,7 +431,7 @@ muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* status = reinterpret_cast<int*>(ws);
-    s = from_cuda(cudaMemsetAsync(status, 0, sizeof(int), st));
+    s = from_cuda(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
     if (s != MUON_OK) return s;
     const int64_t per_chunk = static_cast<int64_t>(ws_bytes) / per;
     const size_t row_bytes = static_cast<size_t>(np) * 2;
@@ -384,7 +456,7 @@ muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t 
                                             cudaMemcpyDeviceToDevice, st));
             if (s != MUON_OK) return s;
         }
-        s = from_cuda(ns_run(&g, 1, ns_steps, a, b, c, status, num_sms, st));
+        s = from_cuda(ns_run(&g, 1, ns_steps, coeffs.data(), status, num_sms, st));
         if (s != MUON_OK) return s;
         const uint16_t* res = g.X[ns_steps & 1];
         for (int64_t k = 0; k < cnt; ++k) {

@@ -5,6 +5,8 @@
 //   normalize_cast  X0 = bf16(u * s) in the wide orientation (smem transpose
 //                   for tall matrices)
 //   final_update    W = W - lr (wd W + scale O)
+//   grad guard      global sum of G^2 and non-finite count; clip factor
+//                   and skip decision
 //   adamw           AdamW on flat buffers
 //
 // Formulas follow "LLM training series, part 2: optimizers" (mhpq.cn):
@@ -34,6 +36,12 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float x) {
 __device__ __forceinline__ float load_g(const void* G, int g_bf16, int64_t i) {
     return g_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(G)[i])
                   : static_cast<const float*>(G)[i];
+}
+
+// The gradient as the momentum sees it: clip * G when global-norm clipping
+// is on (clip read once per CTA from the workspace header), else G.
+__device__ __forceinline__ float scaled_g(float g, int scale_g, float clip) {
+    return scale_g ? __fmul_rn(clip, g) : g;
 }
 
 // Momentum update and Nesterov look-ahead for one element.
@@ -74,6 +82,8 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
     const MatDesc& d = descs[blockIdx.y];
     const int tile = blockIdx.x;
     if (tile >= d.ntiles) return;
+    if (s.header && s.header->skip) return;  // the non-finite guard skips the step
+    const float clip = s.scale_g ? s.header->clip : 1.f;
     const int64_t n = d.rows * d.cols;
     const int64_t start = static_cast<int64_t>(tile) * d.tile_len;
     const int64_t end = min(n, start + d.tile_len);
@@ -106,7 +116,7 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
             float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                float u = momentum_elem(g[j], m[j], s);
+                float u = momentum_elem(scaled_g(g[j], s.scale_g, clip), m[j], s);
                 acc = fmaf(u, u, acc);
             }
             mp[0] = make_float4(m[0], m[1], m[2], m[3]);
@@ -116,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
     }
     for (int64_t i = scalar_from + threadIdx.x; i < end; i += kThreads) {
         float m = M[i];
-        float u = momentum_elem(load_g(G, g_bf16, i), m, s);
+        float u = momentum_elem(scaled_g(load_g(G, g_bf16, i), s.scale_g, clip), m, s);
         M[i] = m;
         acc = fmaf(u, u, acc);
     }
@@ -151,6 +161,8 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const MatDesc*
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTile;
     if (r0 >= rows || c0 >= cols) return;
+    if (s.header && s.header->skip) return;
+    const float clip = s.scale_g ? s.header->clip : 1.f;
     const float scale = d.scale;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const bool full = d.vec && (cols % 4 == 0) && r0 + kTile <= rows && c0 + kTile <= cols;
@@ -180,7 +192,8 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const MatDesc*
             }
             const float m[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = f32_to_bf16(__fmul_rn(lookahead_elem(g[j], m[j], s), scale));
+            for (int j = 0; j < 4; ++j)
+                b[j] = f32_to_bf16(__fmul_rn(lookahead_elem(scaled_g(g[j], s.scale_g, clip), m[j], s), scale));
             if (!tr) {
                 uint2 packed = make_uint2(b[0] | (static_cast<uint32_t>(b[1]) << 16),
                                           b[2] | (static_cast<uint32_t>(b[3]) << 16));
@@ -191,7 +204,8 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const MatDesc*
             for (int j = 0; j < 4; ++j) {
                 if (r < rows && c + j < cols) {
                     const int64_t off = r * cols + c + j;
-                    b[j] = f32_to_bf16(__fmul_rn(lookahead_elem(load_g(G, g_bf16, off), M[off], s), scale));
+                    b[j] = f32_to_bf16(__fmul_rn(
+                        lookahead_elem(scaled_g(load_g(G, g_bf16, off), s.scale_g, clip), M[off], s), scale));
                     if (!tr) X0[r * ldx + c + j] = b[j];
                 }
             }
@@ -240,6 +254,7 @@ __global__ void __launch_bounds__(kThreads) final_update_kernel(const MatDesc* _
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTile;
     if (r0 >= rows || c0 >= cols) return;
+    if (us.header && us.header->skip) return;
     const float sc = d.update_scale;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const bool full = d.vec && (cols % 4 == 0) && r0 + kTile <= rows && c0 + kTile <= cols;
@@ -297,6 +312,109 @@ __global__ void __launch_bounds__(kThreads) final_update_kernel(const MatDesc* _
             }
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// Gradient guard ("LLM training series, part 2: optimizers", section 5.4:
+// skip a step whose gradients hold Inf/NaN; clip by the global norm).
+// ---------------------------------------------------------------------------
+// Each CTA sums kGuardTiles consecutive momentum tiles of one matrix: the
+// sum goes to the first tile's partial, zeros to the others.
+constexpr int kGuardTiles = 4;
+
+__global__ void __launch_bounds__(kThreads) grad_stats_kernel(const MatDesc* __restrict__ descs,
+                                                              WsHeader* __restrict__ header) {
+    __shared__ float red[kThreads / 32];
+    const MatDesc& d = descs[blockIdx.y];
+    const int tile = blockIdx.x * kGuardTiles;
+    if (tile >= d.ntiles) return;
+    const int last = min(d.ntiles, tile + kGuardTiles);
+    const int64_t n = d.rows * d.cols;
+    const int64_t start = static_cast<int64_t>(tile) * d.tile_len;
+    const int64_t end = min(n, static_cast<int64_t>(last) * d.tile_len);
+    const void* G = d.G;
+    const int g_bf16 = d.g_bf16;
+    float acc = 0.f;
+    unsigned int bad = 0;
+    int64_t scalar_from = start;
+    if (d.vec) {
+        const int64_t nvec = (end - start) >> 3;
+        for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
+            const int64_t i = start + (v << 3);
+            float g[8];
+            if (g_bf16) {
+                uint4 raw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(G) + i));
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    g[2 * j] = __uint_as_float(w[j] << 16);
+                    g[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+                }
+            } else {
+                const float4* gp = reinterpret_cast<const float4*>(static_cast<const float*>(G) + i);
+                float4 a = __ldg(gp), b = __ldg(gp + 1);
+                g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+                g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                acc = fmaf(g[j], g[j], acc);
+                bad += isfinite(g[j]) ? 0u : 1u;
+            }
+        }
+        scalar_from = start + (nvec << 3);
+    }
+    for (int64_t i = scalar_from + threadIdx.x; i < end; i += kThreads) {
+        const float g = load_g(G, g_bf16, i);
+        acc = fmaf(g, g, acc);
+        bad += isfinite(g) ? 0u : 1u;
+    }
+    const float total = block_sum(acc, red);
+    if (threadIdx.x == 0) {
+        d.partials[tile] = total;
+        for (int t = tile + 1; t < last; ++t) d.partials[t] = 0.f;
+    }
+    if (bad) atomicAdd(&header->nonfinite, static_cast<unsigned long long>(bad));
+}
+
+// One warp per matrix sums its partials in fp64 (fixed order); one thread
+// then adds the matrix sums to header->sumsq in matrix order, so the total
+// does not depend on scheduling.
+__global__ void __launch_bounds__(kThreads) grad_stats_reduce_kernel(const MatDesc* __restrict__ descs, int count,
+                                                                     WsHeader* __restrict__ header) {
+    constexpr int kBatch = 512;
+    __shared__ double msum[kBatch];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    double total = 0.0;
+    for (int base = 0; base < count; base += kBatch) {
+        const int nb = min(kBatch, count - base);
+        for (int j = warp; j < nb; j += kThreads / 32) {
+            const MatDesc& d = descs[base + j];
+            double s = 0.0;
+            for (int i = lane; i < d.ntiles; i += 32) s += static_cast<double>(d.partials[i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (lane == 0) msum[j] = s;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0)
+            for (int j = 0; j < nb; ++j) total += msum[j];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) header->sumsq += total;
+}
+
+__global__ void grad_decide_kernel(WsHeader* __restrict__ header, float max_grad_norm, int32_t skip_nonfinite) {
+    if (threadIdx.x != 0) return;
+    float clip = 1.f;
+    if (max_grad_norm > 0.f) {
+        const double c = static_cast<double>(max_grad_norm) / (sqrt(header->sumsq) + 1e-6);
+        clip = static_cast<float>(c < 1.0 ? c : 1.0);
+    }
+    header->clip = clip;
+    const int32_t skip = (skip_nonfinite && header->nonfinite > 0) ? 1 : 0;
+    header->skip = skip;
+    if (skip) atomicCAS(&header->status, 0, static_cast<int>(MUON_STEP_SKIPPED));
 }
 
 // ---------------------------------------------------------------------------
@@ -398,6 +516,32 @@ cudaError_t launch_final_update(const MatDesc* descs, int count, int64_t max_row
         final_update_kernel<<<dim3(gx, gy, n), kThreads, 0, st>>>(descs + off, s);
         launch_end(MUON_KERNEL_FINAL_UPDATE, st);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_stats(const MatDesc* descs, int count, int max_tiles, WsHeader* header,
+                              cudaStream_t st) {
+    for (int off = 0; off < count; off += 65535) {
+        int n = count - off < 65535 ? count - off : 65535;
+        launch_begin(MUON_KERNEL_GRAD_GUARD, st);
+        grad_stats_kernel<<<dim3((max_tiles + kGuardTiles - 1) / kGuardTiles, n), kThreads, 0, st>>>(descs + off,
+                                                                                                  header);
+        launch_end(MUON_KERNEL_GRAD_GUARD, st);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_stats_reduce(const MatDesc* descs, int count, WsHeader* header, cudaStream_t st) {
+    launch_begin(MUON_KERNEL_GRAD_GUARD, st);
+    grad_stats_reduce_kernel<<<1, kThreads, 0, st>>>(descs, count, header);
+    launch_end(MUON_KERNEL_GRAD_GUARD, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_decide(WsHeader* header, float max_grad_norm, int32_t skip_nonfinite, cudaStream_t st) {
+    launch_begin(MUON_KERNEL_GRAD_GUARD, st);
+    grad_decide_kernel<<<1, 32, 0, st>>>(header, max_grad_norm, skip_nonfinite);
+    launch_end(MUON_KERNEL_GRAD_GUARD, st);
     return cudaGetLastError();
 }
 

@@ -33,15 +33,28 @@ struct MatDesc {
 
 constexpr int kMaxNormTiles = 1024;
 constexpr size_t kRecordBytes = 8192;     // per matrix, see muon_step.h
-constexpr size_t kHeaderBytes = 256;      // status word lives at offset 0
+constexpr size_t kHeaderBytes = 256;
+
+// Start of the workspace: status word and the gradient guard's results.
+struct WsHeader {
+    int32_t status;               // muon_status_t recorded by kernels
+    int32_t pad0;
+    double sumsq;                 // sum of G^2 over every matrix of the call
+    unsigned long long nonfinite; // non-finite gradient elements
+    float clip;                   // gradient scale (1 when clipping is off)
+    int32_t skip;                 // 1: the non-finite guard skips the step
+};
 
 struct MomentumScalars {
     float mu, one_minus_mu;
     int32_t nesterov;
+    int32_t scale_g;              // 1: multiply G by header->clip first
+    const WsHeader* header;       // guard results (device)
 };
 
 struct UpdateScalars {
     float lr, weight_decay;
+    const WsHeader* header;       // skip flag (device); may be null
 };
 
 struct AdamwScalars {
@@ -65,6 +78,14 @@ cudaError_t launch_final_update(const MatDesc* descs, int count, int64_t max_row
                                 int64_t max_cols, UpdateScalars s, cudaStream_t st);
 cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n,
                          AdamwScalars s, int num_sms, cudaStream_t st);
+// Gradient guard: per-tile sums of G^2 into the partials and a count of
+// non-finite elements into the header; then, per chunk, the partials summed
+// in order into header->sumsq; finally the clip factor and skip flag.
+cudaError_t launch_grad_stats(const MatDesc* descs, int count, int max_tiles, WsHeader* header,
+                              cudaStream_t st);
+cudaError_t launch_grad_stats_reduce(const MatDesc* descs, int count, WsHeader* header, cudaStream_t st);
+cudaError_t launch_grad_decide(WsHeader* header, float max_grad_norm, int32_t skip_nonfinite,
+                               cudaStream_t st);
 
 // ---- Newton-Schulz GEMMs (ns_gemm.cu) -------------------------------------
 // One shape group of wide bf16 matrices in the workspace: `count` matrices,
@@ -85,7 +106,8 @@ constexpr int kNsMaxGroups = 4;
 // group ends in X[steps % 2].  `status` is a device int the kernels set on a
 // bounded-wait timeout.  Returns a CUDA error or cudaSuccess; a tensor-map
 // encoding failure returns cudaErrorInvalidValue.
-cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, float a, float b,
-                   float c, int* status, int num_sms, cudaStream_t st);
+// `coeffs` is host memory of 3 * steps floats, step s using coeffs[3s..3s+2].
+cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, const float* coeffs,
+                   int* status, int num_sms, cudaStream_t st);
 
 }  // namespace muon

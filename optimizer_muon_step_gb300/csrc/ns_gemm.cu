@@ -1195,13 +1195,14 @@ cudaError_t run_stage(const NsGroup* pair_groups, int npair, const NsGroup* sing
 
 }  // namespace
 
-cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, float a, float b, float c, int* status,
-                   int num_sms, cudaStream_t st) {
+cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, const float* coeffs, int* status, int num_sms,
+                   cudaStream_t st) {
     std::vector<NsGroup> pairs, singles;
     for (int i = 0; i < ngroups; ++i) (use_pairs(groups[i]) ? pairs : singles).push_back(groups[i]);
     const int np = static_cast<int>(pairs.size()), ns = static_cast<int>(singles.size());
     for (int s = 0; s < steps; ++s) {
         const int cur = s & 1;
+        const float a = coeffs[3 * s], b = coeffs[3 * s + 1], c = coeffs[3 * s + 2];
         cudaError_t e = run_stage<MODE_SYRK>(pairs.data(), np, singles.data(), ns, cur, a, b, c, status, num_sms, st);
         if (e == cudaSuccess)
             e = run_stage<MODE_POLY>(pairs.data(), np, singles.data(), ns, cur, a, b, c, status, num_sms, st);

@@ -112,6 +112,7 @@ const char* muon_kernel_name(int32_t kind) {
         case MUON_KERNEL_NS_UPDATE: return "ns_update";
         case MUON_KERNEL_FINAL_UPDATE: return "final_update";
         case MUON_KERNEL_ADAMW: return "adamw";
+        case MUON_KERNEL_GRAD_GUARD: return "grad_guard";
     }
     return "unknown";
 }

@@ -49,7 +49,10 @@ class MuonHparams(ctypes.Structure):
                 ("momentum", ctypes.c_float), ("nesterov", ctypes.c_int),
                 ("ns_steps", ctypes.c_int), ("ns_a", ctypes.c_float),
                 ("ns_b", ctypes.c_float), ("ns_c", ctypes.c_float),
-                ("norm_eps", ctypes.c_float), ("rms_scale", ctypes.c_float)]
+                ("norm_eps", ctypes.c_float), ("rms_scale", ctypes.c_float),
+                ("scale_mode", ctypes.c_int), ("skip_nonfinite", ctypes.c_int),
+                ("max_grad_norm", ctypes.c_float), ("reserved", ctypes.c_int),
+                ("ns_coeffs", ctypes.c_void_p)]
 
 
 class AdamwHparams(ctypes.Structure):
@@ -85,16 +88,27 @@ def _load():
             lib.oracle_normalize.argtypes = [P, i64, i64, ctypes.c_float, P]
             lib.oracle_normalize.restype = ctypes.c_float
             lib.oracle_final_update.argtypes = [P, P, i64, i64, ctypes.c_float, ctypes.c_float,
-                                                ctypes.c_float]
+                                                ctypes.c_float, ctypes.c_int]
             lib.oracle_final_update.restype = None
             lib.oracle_muon_step_matrix.argtypes = [P, P, P, i64, i64, P, P, P]
             lib.oracle_muon_step_matrix.restype = ctypes.c_int
+            lib.oracle_muon_step_matrix_scaled.argtypes = [P, P, P, i64, i64, P, ctypes.c_float,
+                                                           ctypes.c_int, P, P]
+            lib.oracle_muon_step_matrix_scaled.restype = ctypes.c_int
+            lib.oracle_newton_schulz_table.argtypes = [P, i64, i64, ctypes.c_int, P, ctypes.c_int]
+            lib.oracle_newton_schulz_table.restype = ctypes.c_int
+            lib.oracle_update_scale.argtypes = [i64, i64, ctypes.c_float, ctypes.c_int]
+            lib.oracle_update_scale.restype = ctypes.c_float
             lib.oracle_adamw_step.argtypes = [P, P, P, P, i64, P, i64]
             lib.oracle_adamw_step.restype = ctypes.c_int
             lib.oracle_ws_bytes_per_matrix.argtypes = [i64, i64]
             lib.oracle_ws_bytes_per_matrix.restype = i64
             lib.oracle_plan.argtypes = [P, P, i64, i64, P]
             lib.oracle_plan.restype = ctypes.c_int
+            lib.oracle_grad_stats.argtypes = [P, P, i64, P, P]
+            lib.oracle_grad_stats.restype = None
+            lib.oracle_clip_factor.argtypes = [ctypes.c_double, ctypes.c_float]
+            lib.oracle_clip_factor.restype = ctypes.c_float
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -143,18 +157,33 @@ CUBIC = (1.5, -0.5, 0.0)  # [OPT] section 4.2: X <- (3X - X X^T X) / 2
 def newton_schulz(X, steps=5, coeffs=QUINTIC, emulate_bf16=True) -> np.ndarray:
     """Run the NS iteration on a wide matrix X (rows <= cols).
 
+    coeffs: one (a, b, c) for every step, or a sequence of `steps` triples.
     emulate_bf16=True: X must hold bf16 values; A, B and each new X are
     rounded to bf16 at the GPU's storage points.  emulate_bf16=False: pure
     fp64, for the closed-form checks."""
     X = np.array(X, dtype=np.float64, order="C", copy=True)
     if X.ndim != 2 or X.shape[0] > X.shape[1]:
         raise ValueError("newton_schulz expects a wide 2-D matrix")
-    a, b, c = (float(np.float32(v)) for v in coeffs)
-    rc = _load().oracle_newton_schulz(_ptr(X), X.shape[0], X.shape[1], int(steps),
-                                      a, b, c, 1 if emulate_bf16 else 0)
+    table = coeff_table(coeffs, steps)
+    rc = _load().oracle_newton_schulz_table(_ptr(X), X.shape[0], X.shape[1], int(steps),
+                                            _ptr(table), 1 if emulate_bf16 else 0)
     if rc:
         raise RuntimeError(f"oracle_newton_schulz failed ({rc})")
     return X
+
+
+def coeff_table(coeffs, steps) -> np.ndarray:
+    """fp32 table of `steps` (a, b, c) triples from one triple or a list."""
+    arr = np.asarray(coeffs, dtype=np.float64)
+    if arr.ndim == 1:
+        arr = np.tile(arr, (max(int(steps), 1), 1))
+    if arr.shape != (max(int(steps), 1), 3) and not (steps == 0):
+        raise ValueError("coeffs must be (a, b, c) or `steps` triples")
+    return np.ascontiguousarray(arr.astype(np.float32).reshape(-1))
+
+
+def update_scale(rows, cols, rms_scale=0.2, scale_mode=0) -> float:
+    return float(_load().oracle_update_scale(int(rows), int(cols), float(rms_scale), int(scale_mode)))
 
 
 # --------------------------------------------------------------------------
@@ -173,15 +202,26 @@ class MuonConfig:
     ns_c: float = QUINTIC[2]
     norm_eps: float = 1e-7
     rms_scale: float = 0.2
+    scale_mode: int = 0            # 0: rms_scale*sqrt(max(m,n)); 1: max(1, sqrt(rows/cols))
+    skip_nonfinite: bool = False   # multi-matrix step: skip when any gradient is non-finite
+    max_grad_norm: float = 0.0     # multi-matrix step: global-norm clip (<= 0: off)
+    ns_coeffs: tuple = None        # None, or ns_steps (a, b, c) triples
 
-    def c_struct(self) -> MuonHparams:
-        return MuonHparams(self.lr, self.weight_decay, self.momentum,
-                           int(bool(self.nesterov)), int(self.ns_steps),
-                           self.ns_a, self.ns_b, self.ns_c, self.norm_eps,
-                           self.rms_scale)
+    def c_struct(self):
+        h = MuonHparams(self.lr, self.weight_decay, self.momentum,
+                        int(bool(self.nesterov)), int(self.ns_steps),
+                        self.ns_a, self.ns_b, self.ns_c, self.norm_eps,
+                        self.rms_scale, int(self.scale_mode), int(bool(self.skip_nonfinite)),
+                        self.max_grad_norm, 0, None)
+        keep = None
+        if self.ns_coeffs is not None:
+            keep = coeff_table(self.ns_coeffs, self.ns_steps)
+            h.ns_coeffs = keep.ctypes.data_as(ctypes.c_void_p)
+        h._keep = keep  # the table must outlive the call
+        return h
 
 
-def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig()):
+def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig(), g_scale: float = 1.0, scale_g: bool = False):
     """One Muon step on one matrix.
 
     W, M: fp32 (rows x cols).  G: fp32 values (a bf16 gradient is passed as
@@ -198,8 +238,10 @@ def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig()):
     X0 = np.empty((mp, np_), dtype=np.float32)
     O = np.empty((mp, np_), dtype=np.float32)
     h = hp.c_struct()
-    rc = _load().oracle_muon_step_matrix(_ptr(W), _ptr(G), _ptr(M), rows, cols,
-                                         ctypes.byref(h), _ptr(X0), _ptr(O))
+    rc = _load().oracle_muon_step_matrix_scaled(_ptr(W), _ptr(G), _ptr(M), rows, cols,
+                                                ctypes.byref(h), float(g_scale),
+                                                1 if g_scale is not None and scale_g else 0,
+                                                _ptr(X0), _ptr(O))
     if rc:
         raise RuntimeError(f"oracle_muon_step_matrix failed ({rc})")
     return W, M, X0, O
@@ -225,7 +267,7 @@ def normalize(u, eps=1e-7):
     return X0.astype(np.float32), float(s)
 
 
-def final_update(W, O, lr=0.02, weight_decay=0.1, rms_scale=0.2):
+def final_update(W, O, lr=0.02, weight_decay=0.1, rms_scale=0.2, scale_mode=0):
     """Step 7 on W (rows x cols) with the wide NS output O; returns new W."""
     W = np.array(W, dtype=np.float32, order="C", copy=True)
     O = np.ascontiguousarray(O, dtype=np.float32)
@@ -233,8 +275,45 @@ def final_update(W, O, lr=0.02, weight_decay=0.1, rms_scale=0.2):
     if O.shape != (min(rows, cols), max(rows, cols)):
         raise ValueError("O must be the wide (min x max) NS output")
     _load().oracle_final_update(_ptr(W), _ptr(O), rows, cols, float(lr), float(weight_decay),
-                                float(rms_scale))
+                                float(rms_scale), int(scale_mode))
     return W
+
+
+def grad_stats(Gs):
+    """(sum of g^2 over all gradients in fp64, count of non-finite elements)."""
+    arrs = [np.ascontiguousarray(g, dtype=np.float32).reshape(-1) for g in Gs]
+    ptrs = (ctypes.c_void_p * max(1, len(arrs)))(*[a.ctypes.data for a in arrs])
+    ns = np.array([a.size for a in arrs] or [0], dtype=np.int64)
+    sumsq = ctypes.c_double(0.0)
+    bad = ctypes.c_int64(0)
+    _load().oracle_grad_stats(ctypes.cast(ptrs, ctypes.c_void_p), _ptr(ns), len(arrs),
+                              ctypes.byref(sumsq), ctypes.byref(bad))
+    return float(sumsq.value), int(bad.value)
+
+
+def clip_factor(sumsq: float, max_norm: float) -> float:
+    return float(_load().oracle_clip_factor(float(sumsq), float(max_norm)))
+
+
+def muon_step_list(Ws, Gs, Ms, hp: MuonConfig = MuonConfig()):
+    """One Muon step over several matrices, with the call-wide gradient
+    guard ([OPT] section 5.4): with skip_nonfinite, any NaN/inf gradient
+    element leaves every matrix unchanged; with max_grad_norm > 0 every
+    gradient is scaled by the global clip factor before the momentum.
+    Returns (list of (W_new, M_new), skipped)."""
+    clip_on = hp.max_grad_norm > 0
+    clip = 1.0
+    if clip_on or hp.skip_nonfinite:
+        sumsq, bad = grad_stats(Gs)
+        if hp.skip_nonfinite and bad > 0:
+            return [(np.array(W, np.float32), np.array(M, np.float32)) for W, M in zip(Ws, Ms)], True
+        if clip_on:
+            clip = clip_factor(sumsq, hp.max_grad_norm)
+    out = []
+    for W, G, M in zip(Ws, Gs, Ms):
+        W1, M1, _, _ = muon_step_matrix(W, G, M, hp, g_scale=clip, scale_g=clip_on)
+        out.append((W1, M1))
+    return out, False
 
 
 # --------------------------------------------------------------------------

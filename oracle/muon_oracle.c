@@ -117,7 +117,8 @@ static void transpose_f64(const double* X, double* XT, int64_t R, int64_t C)
 /* Newton-Schulz orthogonalisation                                           */
 /* ------------------------------------------------------------------------ */
 
-/* One odd matrix polynomial applied `steps` times to a wide X (rows <= cols):
+/* One odd matrix polynomial applied `steps` times to a wide X (rows <= cols),
+ * step s with its own coefficients (a, b, c) = coeffs[3s .. 3s+2]:
  *     A  = X X^T
  *     B  = b A + c A A
  *     X <- a X + B X
@@ -133,10 +134,10 @@ static void transpose_f64(const double* X, double* XT, int64_t R, int64_t C)
  *       X = bf16( fl32(a*X) + float(B X) )
  * emulate_bf16 == 0: everything stays in fp64 (used to check the iteration
  *   against its singular-value closed form). */
-int oracle_newton_schulz(double* X, int64_t rows, int64_t cols, int steps,
-                         float a, float b, float c, int emulate_bf16)
+int oracle_newton_schulz_table(double* X, int64_t rows, int64_t cols, int steps,
+                               const float* coeffs, int emulate_bf16)
 {
-    if (rows <= 0 || cols <= 0 || steps < 0 || rows > cols)
+    if (rows <= 0 || cols <= 0 || steps < 0 || rows > cols || (steps > 0 && !coeffs))
         return 1;
     double* XT = (double*)malloc(sizeof(double) * rows * cols);
     double* A = (double*)malloc(sizeof(double) * rows * rows);
@@ -148,6 +149,7 @@ int oracle_newton_schulz(double* X, int64_t rows, int64_t cols, int steps,
         return 2;
     }
     for (int s = 0; s < steps; ++s) {
+        const float a = coeffs[3 * s], b = coeffs[3 * s + 1], c = coeffs[3 * s + 2];
         /* A = X X^T */
         transpose_f64(X, XT, rows, cols);
         matmul_f64(X, XT, A, rows, cols, rows);
@@ -180,6 +182,21 @@ int oracle_newton_schulz(double* X, int64_t rows, int64_t cols, int steps,
     return 0;
 }
 
+/* The same iteration with one coefficient triple for every step. */
+int oracle_newton_schulz(double* X, int64_t rows, int64_t cols, int steps,
+                         float a, float b, float c, int emulate_bf16)
+{
+    if (steps < 0 || steps > 100)
+        return 1;
+    float table[300];
+    for (int s = 0; s < steps; ++s) {
+        table[3 * s] = a;
+        table[3 * s + 1] = b;
+        table[3 * s + 2] = c;
+    }
+    return oracle_newton_schulz_table(X, rows, cols, steps, table, emulate_bf16);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Muon step for one matrix                                                  */
 /* ------------------------------------------------------------------------ */
@@ -193,25 +210,40 @@ typedef struct {
     float ns_a, ns_b, ns_c;
     float norm_eps;     /* added to the Frobenius norm                      */
     float rms_scale;    /* update scale = rms_scale * sqrt(max(rows, cols)) */
+    int scale_mode;     /* 0: rms_scale * sqrt(max(rows, cols));
+                           1: max(1, sqrt(rows / cols))                     */
+    int skip_nonfinite; /* used by the multi-matrix step (Python side)      */
+    float max_grad_norm;/* used by the multi-matrix step (Python side)      */
+    int reserved;
+    const float* ns_coeffs; /* NULL, or 3 * ns_steps per-step coefficients  */
 } oracle_muon_hparams;
 
-/* Steps 1-2 of the Muon step, element by element, in place on M:
+/* Steps 1-2 of the Muon step, element by element, in place on M.  With
+ * scale_g != 0 the gradient is first multiplied by g_scale in fp32 (the
+ * global-norm clip factor of the multi-matrix step):
  *  1. momentum, an exponential moving average of the gradient
  *     ([OPT] section 2.1):   M = fl(fl(mu*M) + fl((1-mu)*G))
  *  2. Nesterov look-ahead, read as the same average taken one step further:
  *        u = fl(fl((1-mu)*G) + fl(mu*M))        (nesterov = 1)
  *        u = M                                   (nesterov = 0)
  * (1-mu) is computed in fp32.  u may be NULL. */
-void oracle_momentum(const float* G, float* M, float* u, int64_t n, float mu, int nesterov)
+void oracle_momentum_scaled(const float* G, float* M, float* u, int64_t n, float mu, int nesterov,
+                            float g_scale, int scale_g)
 {
     const float one_minus_mu = 1.0f - mu;
     for (int64_t i = 0; i < n; ++i) {
-        float gterm = one_minus_mu * G[i];
+        const float g = scale_g ? g_scale * G[i] : G[i];
+        float gterm = one_minus_mu * g;
         float mnew = mu * M[i] + gterm;
         M[i] = mnew;
         if (u)
             u[i] = nesterov ? gterm + mu * mnew : mnew;
     }
+}
+
+void oracle_momentum(const float* G, float* M, float* u, int64_t n, float mu, int nesterov)
+{
+    oracle_momentum_scaled(G, M, u, n, mu, nesterov, 1.0f, 0);
 }
 
 /* Steps 3-4: Frobenius normalisation and bf16 rounding.
@@ -239,18 +271,34 @@ float oracle_normalize(const float* u, int64_t rows, int64_t cols, float eps, do
     return s;
 }
 
+/* The update's scale factor, computed in fp64 and rounded to fp32:
+ *   mode 0: rms_scale * sqrt(max(rows, cols)) -- the update RMS matches
+ *           AdamW's 0.2-0.4 ([K2] section 3.1);
+ *   mode 1: max(1, sqrt(d_out / d_in)) = max(1, sqrt(rows / cols)) for an
+ *           (out, in) weight -- the per-matrix learning-rate adjustment of
+ *           the muP view ([K2] section 3.2). */
+float oracle_update_scale(int64_t rows, int64_t cols, float rms_scale, int scale_mode)
+{
+    if (scale_mode == 1) {
+        double r = sqrt((double)rows / (double)cols);
+        return (float)(r > 1.0 ? r : 1.0);
+    }
+    const int64_t np = rows > cols ? rows : cols;
+    return (float)((double)rms_scale * sqrt((double)np));
+}
+
 /* Step 7: decoupled weight decay and the RMS-matched update ([OPT] section
  * 3.1 for the decoupled form, [K2] section 3.1 for matching the update RMS
  * of AdamW).  Both terms use the old W:
- *    scale = float(rms_scale * sqrt(max(rows, cols)))     (fp64 -> fp32)
+ *    scale = oracle_update_scale(rows, cols, rms_scale, scale_mode)
  *    W = fl(W - fl(lr * fl(fl(wd*W) + fl(scale*O))))
  * O is the NS output in the wide orientation (min x max, float values). */
 void oracle_final_update(float* W, const float* O, int64_t rows, int64_t cols,
-                         float lr, float weight_decay, float rms_scale)
+                         float lr, float weight_decay, float rms_scale, int scale_mode)
 {
     const int transposed = rows > cols;
     const int64_t np = transposed ? rows : cols;
-    const float scale = (float)((double)rms_scale * sqrt((double)np));
+    const float scale = oracle_update_scale(rows, cols, rms_scale, scale_mode);
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c) {
             float o = transposed ? O[c * np + r] : O[r * np + c];
@@ -263,8 +311,9 @@ void oracle_final_update(float* W, const float* O, int64_t rows, int64_t cols,
 }
 
 /* One Muon step on one rows x cols matrix, in place on W and M:
- * oracle_momentum, oracle_normalize, NS (oracle_newton_schulz with bf16
- * emulation) on the wide matrix, oracle_final_update.
+ * oracle_momentum (on g_scale * G when scale_g != 0), oracle_normalize, NS
+ * (bf16 emulation; per-step coefficients when hp->ns_coeffs is set) on the
+ * wide matrix, oracle_final_update.
  *   W   fp32 master weight (rows x cols, row-major), updated in place
  *   G   gradient, fp32 values (a bf16 gradient is passed already widened:
  *       the widening is exact)
@@ -272,10 +321,11 @@ void oracle_final_update(float* W, const float* O, int64_t rows, int64_t cols,
  *   X0  optional out: the normalised bf16 NS input (wide, float values)
  *   O   optional out: the NS output (wide, float values)
  * Returns 0 on success. */
-int oracle_muon_step_matrix(float* W, const float* G, float* M,
-                            int64_t rows, int64_t cols,
-                            const oracle_muon_hparams* hp,
-                            float* X0_out, float* O_out)
+int oracle_muon_step_matrix_scaled(float* W, const float* G, float* M,
+                                   int64_t rows, int64_t cols,
+                                   const oracle_muon_hparams* hp,
+                                   float g_scale, int scale_g,
+                                   float* X0_out, float* O_out)
 {
     if (rows <= 0 || cols <= 0 || !hp)
         return 1;
@@ -289,13 +339,14 @@ int oracle_muon_step_matrix(float* W, const float* G, float* M,
         free(u); free(X); free(O);
         return 2;
     }
-    oracle_momentum(G, M, u, n, hp->momentum, hp->nesterov);
+    oracle_momentum_scaled(G, M, u, n, hp->momentum, hp->nesterov, g_scale, scale_g);
     oracle_normalize(u, rows, cols, hp->norm_eps, X);
     if (X0_out)
         for (int64_t i = 0; i < n; ++i)
             X0_out[i] = (float)X[i];
-    int rc = oracle_newton_schulz(X, mp, np, hp->ns_steps, hp->ns_a, hp->ns_b,
-                                  hp->ns_c, 1);
+    int rc = hp->ns_coeffs
+                 ? oracle_newton_schulz_table(X, mp, np, hp->ns_steps, hp->ns_coeffs, 1)
+                 : oracle_newton_schulz(X, mp, np, hp->ns_steps, hp->ns_a, hp->ns_b, hp->ns_c, 1);
     if (rc) {
         free(u); free(X); free(O);
         return 10 + rc;
@@ -304,9 +355,45 @@ int oracle_muon_step_matrix(float* W, const float* G, float* M,
         O[i] = (float)X[i];
     if (O_out)
         memcpy(O_out, O, sizeof(float) * n);
-    oracle_final_update(W, O, rows, cols, hp->lr, hp->weight_decay, hp->rms_scale);
+    oracle_final_update(W, O, rows, cols, hp->lr, hp->weight_decay, hp->rms_scale, hp->scale_mode);
     free(u); free(X); free(O);
     return 0;
+}
+
+int oracle_muon_step_matrix(float* W, const float* G, float* M,
+                            int64_t rows, int64_t cols,
+                            const oracle_muon_hparams* hp,
+                            float* X0_out, float* O_out)
+{
+    return oracle_muon_step_matrix_scaled(W, G, M, rows, cols, hp, 1.0f, 0, X0_out, O_out);
+}
+
+/* Statistics of all gradients of one multi-matrix step ([OPT] section 5.4:
+ * an Inf guard that skips the step, and clipping by the global norm):
+ * *sumsq = sum of g^2 over every element of every matrix, in fp64, matrix by
+ * matrix in element order; *nonfinite = number of NaN or +-inf elements. */
+void oracle_grad_stats(const float* const* G, const int64_t* n, int64_t count,
+                       double* sumsq, int64_t* nonfinite)
+{
+    double s = 0.0;
+    int64_t bad = 0;
+    for (int64_t k = 0; k < count; ++k)
+        for (int64_t i = 0; i < n[k]; ++i) {
+            const double g = (double)G[k][i];
+            s += g * g;
+            if (!isfinite(G[k][i]))
+                ++bad;
+        }
+    *sumsq = s;
+    *nonfinite = bad;
+}
+
+/* The clip factor: min(1, max_norm / (sqrt(sumsq) + 1e-6)) in fp64, rounded
+ * to fp32 (a NaN ratio gives 1). */
+float oracle_clip_factor(double sumsq, float max_norm)
+{
+    const double c = (double)max_norm / (sqrt(sumsq) + 1e-6);
+    return (float)(c < 1.0 ? c : 1.0);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -156,11 +156,34 @@ def test_adamw_argument_validation(built):
 def test_newton_schulz_argument_validation(built):
     lib = built
     P = ctypes.c_void_p
-    f = ctypes.c_float
-    # tall input is rejected, count 0 is a no-op
-    assert lib.muon_newton_schulz(P(1024), P(2048), 1, 8, 4, 5, f(1), f(1), f(1), P(4096), 1 << 20, None) == 1
-    assert lib.muon_newton_schulz(None, None, 0, 4, 8, 5, f(1), f(1), f(1), None, 0, None) == 0
-    assert lib.muon_newton_schulz(P(1024), P(2048), 1, 4, 8, 5, f(1), f(1), f(1), P(4096), 16, None) == 4
+    one = (ctypes.c_float * 3)(1.0, 1.0, 1.0)
+    c = ctypes.cast(one, P)
+    # tall input is rejected, count 0 is a no-op, a small workspace is rejected
+    assert lib.muon_newton_schulz(P(1024), P(2048), 1, 8, 4, 5, c, 1, P(4096), 1 << 20, None) == 1
+    assert lib.muon_newton_schulz(None, None, 0, 4, 8, 5, c, 1, None, 0, None) == 0
+    assert lib.muon_newton_schulz(P(1024), P(2048), 1, 4, 8, 5, c, 1, P(4096), 16, None) == 4
+    # the coefficient table has one triple or one per step
+    assert lib.muon_newton_schulz(P(1024), P(2048), 1, 4, 8, 5, c, 2, P(4096), 1 << 20, None) == 1
+    assert lib.muon_newton_schulz(P(1024), P(2048), 1, 4, 8, 5, None, 1, P(4096), 1 << 20, None) == 1
+    bad = (ctypes.c_float * 3)(1.0, float("inf"), 1.0)
+    assert lib.muon_newton_schulz(P(1024), P(2048), 1, 4, 8, 1, ctypes.cast(bad, P), 1, P(4096), 1 << 20,
+                                  None) == 1
+
+
+def test_step_new_hparam_validation(built):
+    lib = built
+    arr = (m.MuonMatrix * 1)()
+    arr[0].W = arr[0].G = arr[0].M = 1024
+    arr[0].rows, arr[0].cols = 4, 4
+    ws = ctypes.c_void_p(4096)
+    for field, value in (("scale_mode", 2), ("skip_nonfinite", 3), ("reserved0", 1),
+                         ("max_grad_norm", float("nan"))):
+        h = _hp()
+        setattr(h, field, value)
+        assert lib.muon_step_batched(arr, 1, ctypes.byref(h), ws, 1 << 20, None) == 1, field
+    bad = m.MuonHparams(ns_steps=2, ns_coeffs=[(1.5, -0.5, 0.0), (1.5, float("nan"), 0.0)])._c()
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(bad), ws, 1 << 20, None) == 1
+    assert built.muon_status_string(8) == b"step skipped by the non-finite gradient guard"
 
 
 def test_library_never_loads_the_oracle(built):

@@ -415,3 +415,87 @@ def test_stage_functions_compose_to_the_step():
     assert np.array_equal(M1, M2) and np.array_equal(X0, X0b)
     assert np.array_equal(O, Ob) and np.array_equal(W1, W2)
     assert s > 0 and abs(np.linalg.norm(u.astype(np.float64)) * s - 1) < 1e-6
+
+
+
+# --------------------------------------------------------------------------
+# Next rows: per-step NS coefficients, the muP update scale, the gradient
+# guard
+# --------------------------------------------------------------------------
+
+def test_ns_per_step_coefficients_compose_scalar_maps():
+    """With a different (a, b, c) at each step NS still acts on each
+    singular value independently: the result is U (p_k o ... o p_1)(S) V^T."""
+    table = [(1.5, -0.5, 0.0), QUINTIC, (1.5, -0.5, 0.0), (2.0, -1.5, 0.5)]
+    X = rand_wide(12, 30, seed=4)
+    U, S, Vt = np.linalg.svd(X, full_matrices=False)
+    s = S.copy()
+    for a, b, c in (tuple(float(np.float32(v)) for v in t) for t in table):
+        s = a * s + b * s ** 3 + c * s ** 5
+    got = oracle.newton_schulz(X, steps=len(table), coeffs=table, emulate_bf16=False)
+    assert np.linalg.norm(got - (U * s) @ Vt) / np.linalg.norm(got) < 1e-10
+    # a table repeating one triple equals that triple
+    Xb = oracle.bf16_round(rand_wide(16, 48, seed=5))
+    assert np.array_equal(oracle.newton_schulz(Xb, 3, [QUINTIC] * 3), oracle.newton_schulz(Xb, 3, QUINTIC))
+
+
+def test_mup_scale_mode():
+    """[K2] section 3.2: the per-matrix adjustment max(1, sqrt(d_out/d_in)):
+    1 for wide or square (out <= in) weights, sqrt(out/in) for tall ones;
+    and mode 0 is 0.2 * sqrt(max(m, n))."""
+    assert oracle.update_scale(2048, 2048, 0.2, 1) == 1.0
+    assert oracle.update_scale(1024, 4096, 0.2, 1) == 1.0
+    assert oracle.update_scale(4096, 1024, 0.2, 1) == 2.0
+    assert oracle.update_scale(256, 512, 0.2, 0) == np.float32(0.2 * math.sqrt(512))
+    # the step's update uses it: with wd = 0, dW = -lr * 2 * O for a 4:1 tall matrix
+    W, G, M = _inputs(64, 16, 9)
+    hp = oracle.MuonConfig(weight_decay=0.0, scale_mode=1)
+    W1, _, _, O = oracle.muon_step_matrix(W, G, M, hp)
+    dW = W1.astype(np.float64) - W
+    assert np.allclose(dW, -float(np.float32(hp.lr)) * 2.0 * O.T.astype(np.float64), rtol=1e-5, atol=1e-9)
+
+
+def test_grad_guard_skips_on_nonfinite():
+    """[OPT] section 5.4: an anomaly anywhere skips the whole step."""
+    mats = [_inputs(8, 12, 20 + i) for i in range(3)]
+    Ws, Gs, Ms = [m[0] for m in mats], [m[1].copy() for m in mats], [m[2] for m in mats]
+    Gs[1][2, 3] = np.inf
+    out, skipped = oracle.muon_step_list(Ws, Gs, Ms, oracle.MuonConfig(skip_nonfinite=True))
+    assert skipped
+    for (W1, M1), W, M in zip(out, Ws, Ms):
+        assert np.array_equal(W1, W) and np.array_equal(M1, M)
+    s, bad = oracle.grad_stats(Gs)
+    assert bad == 1 and s == np.inf
+
+
+def test_grad_clip_bounds_the_global_norm():
+    """Clipping scales every gradient by one factor so the global norm is
+    max_grad_norm: from M = 0 the new momentum is (1-mu) clip G, whose global
+    norm is (1-mu) * max_grad_norm."""
+    mats = [_inputs(16, 24, 30 + i, g_std=1.0) for i in range(3)]
+    Ws, Gs = [m[0] for m in mats], [m[1] for m in mats]
+    Ms = [np.zeros_like(m[2]) for m in mats]
+    norm = math.sqrt(sum(float((g.astype(np.float64) ** 2).sum()) for g in Gs))
+    hp = oracle.MuonConfig(max_grad_norm=norm / 3, momentum=0.5)
+    out, skipped = oracle.muon_step_list(Ws, Gs, Ms, hp)
+    assert not skipped
+    got = math.sqrt(sum(float((M1.astype(np.float64) ** 2).sum()) for _, M1 in out))
+    assert abs(got - 0.5 * norm / 3) / (0.5 * norm / 3) < 1e-6
+
+
+def test_grad_clip_inactive_below_threshold_and_direction_only_above():
+    """Below the threshold the clip factor is exactly 1 (results identical
+    to no clipping); above it the clipped gradient depends only on the
+    gradient's direction, so doubling every gradient changes nothing."""
+    mats = [_inputs(16, 24, 40 + i) for i in range(2)]
+    Ws, Gs, Ms = [m[0] for m in mats], [m[1] for m in mats], [m[2] for m in mats]
+    plain, _ = oracle.muon_step_list(Ws, Gs, Ms, oracle.MuonConfig())
+    loose, _ = oracle.muon_step_list(Ws, Gs, Ms, oracle.MuonConfig(max_grad_norm=1e9))
+    for (a, b), (c, d) in zip(plain, loose):
+        assert np.array_equal(a, c) and np.array_equal(b, d)
+    hp = oracle.MuonConfig(max_grad_norm=1e-3)
+    one, _ = oracle.muon_step_list(Ws, Gs, Ms, hp)
+    two, _ = oracle.muon_step_list(Ws, [2 * g for g in Gs], Ms, hp)
+    for (W1, M1), (W2, M2) in zip(one, two):
+        assert np.allclose(M1, M2, rtol=1e-6, atol=0)
+        assert np.allclose(W1, W2, rtol=1e-6, atol=1e-9)
