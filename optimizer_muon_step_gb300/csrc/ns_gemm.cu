@@ -3,17 +3,21 @@
 // One step of the odd matrix polynomial on a batch of wide bf16 matrices X
 // (m' x n', m' <= n'), as three grouped GEMM launches:
 //
-//   SYRK    A = X X^T            upper-triangle tiles only, mirrored on store
-//   POLY    B = b A + c (A A)    upper-triangle tiles only, mirrored on store
+//   SYRK    A = X X^T            tiles of the upper block band only
+//   POLY    B = b A + c (A A)    tiles of the upper block band only
 //   UPDATE  X' = a X + B X       all tiles
 //
 // The iteration is the one "LLM training series, part 2: optimizers"
 // (mhpq.cn, section 4.2) describes: it pushes the singular values of X
 // towards 1 without an SVD.  The cubic member there is (a, b, c) =
 // (1.5, -0.5, 0); the library's default is the quintic (3.4445, -4.7750,
-// 2.0315).  A and B are symmetric, so SYRK and POLY compute only tiles that
-// touch the upper triangle and store each element twice (A[r][c] and
-// A[c][r]); elements strictly below the diagonal come from their mirror.
+// 2.0315).  A and B are symmetric, so SYRK and POLY compute and store only
+// the upper block band: with row blocks of S rows (S = 128 on single CTAs,
+// 256 on CTA pairs), block (p, q) is stored when q >= p, diagonal blocks in
+// full.  A consumer reading rows of block p along k takes the k-blocks of
+// blocks q >= p as stored (K-major) and those of q < p from the transposed
+// position (block (q, p), read MN-major): A[r][k] = A[k][r].  Nothing is
+// stored twice and nothing below the band is ever read.
 //
 // Two kernels share the epilogue: a single-CTA kernel on 128x256 tiles and
 // a CTA-pair kernel (tcgen05 cta_group::2) on 256x256 pair tiles, chosen per
@@ -26,10 +30,12 @@
 //                M=128 N=256 K=16, fp32 accumulators in TMEM, two 256-column
 //                accumulator buffers so the epilogue of one tile overlaps the
 //                main loop of the next
-//   warps 2..5   epilogue: tcgen05.ld 32 lanes x 32 columns, fused
-//                polynomial / update arithmetic in fp32, bf16 stores
-// All operands are K-major except UPDATE's B operand (X read along its
-// rows, i.e. MN-major), which the descriptor's transpose bit handles, so no
+//   warps 2..5   epilogue, one warp per TMEM lane quarter: tcgen05.ld 32
+//                lanes x 32 columns, fused polynomial / update arithmetic
+//                in fp32, 32x64 bf16 blocks in and out through TMA
+// X is read K-major by SYRK and MN-major by UPDATE (its B operand); A and B
+// are read K-major or MN-major per k-block as above.  The instruction
+// descriptor's per-operand major bits select the layout per MMA, so no
 // matrix is ever transposed in memory.  Every wait is bounded: after
 // ~2 seconds a CTA records MUON_ERR_TIMEOUT, drains what it issued, frees
 // its TMEM and exits.
@@ -58,8 +64,14 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = MUON_EPI_WARPS;  // 4 or 8; two warps per TMEM lane quarter when 8
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;  // two BN-column fp32 accumulators
-constexpr int EBUF_BYTES = 32 * 32 * 2;                  // one 32x32 bf16 block
-constexpr int NSLOT = 4;                                   // block buffers per epilogue warp
+#ifndef MUON_EPI_COLS
+#define MUON_EPI_COLS 64
+#endif
+constexpr int EPI_COLS = MUON_EPI_COLS;                    // columns of one epilogue block: 32 or 64
+constexpr int EROW_BYTES = EPI_COLS * 2;                   // one block row, bf16; also its swizzle span
+constexpr int EBUF_BYTES = 32 * EROW_BYTES;                // one 32-row bf16 block
+constexpr int NSLOT = 32768 / (EPI_WARPS * EBUF_BYTES);    // block buffers per epilogue warp (32 KB in all)
+constexpr int MN_CHUNK_BYTES = 64 * BK * 2;                // one 64-row chunk of an MN-major operand
 constexpr int EBUFS_BYTES = EPI_WARPS * NSLOT * EBUF_BYTES;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EBUFS_BYTES + 256;
 constexpr unsigned long long kDrainNs = 500000000ull;
@@ -67,12 +79,19 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 enum Mode { MODE_SYRK = 0, MODE_POLY = 1, MODE_UPDATE = 2 };
 
+// MN-major operands (64-row chunks of the M or N dimension, each 64 k-rows
+// of 128 bytes, 8 KB apart) are loaded one of two ways.  A "chunked" map
+// views a row-major matrix whose width is a multiple of 64 as
+// [matrix][chunk][row][64 elements] (chunk stride 128 bytes), so a single
+// box {64, 64, C} brings C chunks in one copy; other widths take one
+// {64, 64} box per chunk from a plain 3-D map.  Fewer, larger copies keep
+// the TMA unit ahead of the tensor core.
 struct GroupParams {
     CUtensorMap tm_a;      // A operand: rows of the left factor, K-major, box {64, 128}
-    CUtensorMap tm_b;      // B operand: K-major box {64, 256} or MN-major box {64, 64}
-    CUtensorMap tm_e;      // epilogue addend, box {32, 32}, 64-byte swizzle
-    CUtensorMap tm_d;      // output block store, box {32, 32}, 64-byte swizzle
-    CUtensorMap tm_m;      // mirror block store, box {32, 32}, no swizzle
+    CUtensorMap tm_b;      // B operand: K-major box {64, 256} (pairs {64, 128}); UPDATE: X MN-major
+    CUtensorMap tm_t;      // symmetric factor read MN-major (transposed position), 2 chunks per copy
+    CUtensorMap tm_e;      // epilogue addend, box {EPI_COLS, 32}, swizzled over the row
+    CUtensorMap tm_d;      // output block store, box {EPI_COLS, 32}, swizzled over the row
     const uint16_t* E;     // epilogue addend (POLY: A, UPDATE: X)
     uint16_t* D;           // output
     int64_t ld;            // row stride of D and E, elements
@@ -82,7 +101,7 @@ struct GroupParams {
     int32_t tiles_n;
     int32_t tiles_per_mat;
     int32_t tile_begin;
-    int32_t pad_;
+    int32_t chunked;       // MN-major maps are chunked (4-D); else plain 3-D {64, 64} boxes
 };
 
 struct NsParams {
@@ -170,6 +189,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
 }
 
@@ -265,11 +293,43 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
-// and B (bits 7-9, 10-12 = 1), B major-ness (bit 16), N >> 3 (bits 17-22),
-// M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t instr_desc(int m, int n, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+// and B (bits 7-9, 10-12 = 1), A and B major-ness (bits 15, 16), N >> 3
+// (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t instr_desc(int m, int n, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Descriptor of the k-th 16-deep slice of an operand staged by one k-block
+// load.  K-major: 128-byte rows of 64 k, 8-row groups 1024 bytes apart.
+// MN-major: 64-element chunks of rows 8 KB apart, each 64 k-rows of 128
+// bytes.  In both layouts row r of the operand starts r * 128 bytes in
+// (for r a multiple of 64), which the caller adds to `base`.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int k, bool mn_major) {
+    return mn_major ? smem_desc(base + static_cast<uint32_t>(k) * 16 * 128, MN_CHUNK_BYTES, 1024)
+                    : smem_desc(base + static_cast<uint32_t>(k) * 32, 16, 1024);
+}
+
+// Whether rows of row block `row_block` read k-block kb (64 wide) of a
+// symmetric factor from the transposed position: blocks of 2^shift k-blocks.
+__device__ __forceinline__ bool read_transposed(int kb, int row_block, int shift) {
+    return (kb >> shift) < row_block;
+}
+
+// Copies of an MN-major operand covering rows [r0, r0 + 64 * nchunks) at
+// k-block kb, chunk c landing at dst + c * 8 KB: `per_copy` chunks per copy
+// from a chunked map (r0 a multiple of 64), or one {64, 64} box per chunk.
+// LOAD3/LOAD4 issue a 3-D / 4-D tensor copy.
+template <typename Load3, typename Load4>
+__device__ __forceinline__ void load_mn(uint32_t dst, const CUtensorMap* map, bool chunked, int per_copy, int r0,
+                                        int nchunks, int kb, int mat, Load3 load3, Load4 load4) {
+    if (chunked) {
+        for (int c = 0; c < nchunks; c += per_copy)
+            load4(dst + static_cast<uint32_t>(c) * MN_CHUNK_BYTES, map, 0, kb * BK, (r0 >> 6) + c, mat);
+    } else {
+        for (int c = 0; c < nchunks; ++c)
+            load3(dst + static_cast<uint32_t>(c) * MN_CHUNK_BYTES, map, r0 + 64 * c, kb * BK, mat);
+    }
 }
 
 struct Tile {
@@ -341,12 +401,10 @@ __device__ __forceinline__ void chunk_values(const float (&v)[32], const uint4 (
     }
 }
 
-__device__ __forceinline__ uint16_t to_bf16(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-
 // Per-warp state of the epilogue's bulk copies; lives across tiles.  Each
-// epilogue warp owns NSLOT 2 KB block buffers (64-byte swizzle): the first
-// RING slots hold the addend-in / output-out ring, and for SYRK/POLY slots 2
-// and 3 alternate as mirror staging.
+// epilogue warp owns a ring of NSLOT block buffers (32 rows x EPI_COLS,
+// swizzled over the row length: 64 or 128 bytes);
+// a slot takes a block's addend in and the finished block out.
 struct EpiBufs {
     uint32_t buf[NSLOT];    // shared::cta addresses
     uint8_t* ptr[NSLOT];    // the same buffers as generic pointers
@@ -356,159 +414,107 @@ struct EpiBufs {
     uint32_t seq;           // blocks this warp has written so far (all tiles)
 };
 
-// Ring of addend/output slots per stage and how many blocks ahead the
-// addend is loaded (measured on the dense-decoder workload; a slot is
-// reused once the bulk group RING-AHEAD blocks back has been read).
-#ifndef MUON_RING_UPDATE
-#define MUON_RING_UPDATE 2
+// How many blocks ahead of its use a block's addend is requested.  A slot
+// is reused once the bulk group NSLOT - AHEAD blocks back has been read.
+#ifndef MUON_EPI_AHEAD
+#define MUON_EPI_AHEAD NSLOT
 #endif
-#ifndef MUON_AHEAD_UPDATE
-#define MUON_AHEAD_UPDATE 2
-#endif
-#ifndef MUON_RING_SYM
-#define MUON_RING_SYM 2
-#endif
-#ifndef MUON_AHEAD_SYM
-#define MUON_AHEAD_SYM 2
-#endif
-template <int MODE>
-struct EpiRing {
-    static constexpr int kRing = MODE == MODE_UPDATE ? MUON_RING_UPDATE : MUON_RING_SYM;
-    static constexpr int kAhead = MODE == MODE_UPDATE ? MUON_AHEAD_UPDATE : MUON_AHEAD_SYM;
-    static_assert(kAhead >= 1 && kAhead <= kRing, "addend distance must fit the ring");
-    static_assert(kRing + (MODE == MODE_UPDATE ? 0 : 2) <= NSLOT, "ring and mirror slots exceed NSLOT");
-};
+constexpr int EPI_AHEAD = MUON_EPI_AHEAD;
+static_assert(EPI_AHEAD >= 1 && EPI_AHEAD <= NSLOT, "addend distance must fit the ring");
 
-// Waits for the accumulator, then writes the tile, 32x32 blocks at a time.
-//   addend (POLY: A, UPDATE: X): bulk tensor load into a slot of the ring,
-//     requested kAhead blocks ahead; the first ones before the accumulator
-//     wait so they overlap the main loop;
+// Waits for the accumulator, then writes the warp's share of the tile,
+// 32x32 blocks at a time:
+//   addend (POLY: A, UPDATE: X): bulk tensor load into a ring slot,
+//     requested EPI_AHEAD blocks ahead; the first ones before the
+//     accumulator wait so they overlap the main loop;
 //   output: each lane writes its row of the finished block into the same
-//     slot (same swizzle) and one lane issues a bulk tensor store; the
-//     mirror block of SYRK/POLY goes through a transposed staging slot and a
-//     second bulk store in the same bulk group.  Rows or columns past the
-//     matrix are clipped by the tensor store.  A slot is reused only after
-//     the bulk group that read it (two groups back) has finished reading;
-//   diagonal blocks of SYRK/POLY (col0 == row_base) are written element by
-//     element, so each element of the symmetric output has exactly one
-//     writer.
+//     slot (same swizzle) and one lane issues a bulk tensor store.  Rows or
+//     columns past the matrix are clipped by the tensor store.
+// Blocks left of `col_min` (SYRK/POLY: the first column of the tile's row
+// block) lie below the stored band and are neither computed nor written.
 // Returns false when the CTA is aborting.
 template <int MODE>
 __device__ __forceinline__ bool epilogue_tile(const NsParams& p, const GroupParams& g, const Tile& tile,
-                                              uint32_t t_acc, int quarter, int half, int lane, uint32_t tfull,
-                                              uint32_t acc_phase, volatile int* abort_flag, EpiBufs& eb) {
-    constexpr int CH = BN / 32 / (EPI_WARPS / 4);  // blocks of 32 columns this warp writes
-    constexpr int RING = EpiRing<MODE>::kRing;
-    constexpr int AHEAD = EpiRing<MODE>::kAhead;
+                                              int col_min, uint32_t t_acc, int quarter, int half, int lane,
+                                              uint32_t tfull, uint32_t acc_phase, volatile int* abort_flag,
+                                              EpiBufs& eb) {
+    constexpr int CH = BN / EPI_COLS / (EPI_WARPS / 4);  // blocks of EPI_COLS columns this warp writes
     const int row_base = tile.ti * BM + quarter * 32;
-    const int row = row_base + lane;
-    const int64_t mat_off = static_cast<int64_t>(tile.mat) * g.bs;
-    uint16_t* __restrict__ D = g.D + mat_off;
-    const int col_base = tile.tj * BN + half * CH * 32;
+    const int col_base = tile.tj * BN + half * CH * EPI_COLS;
     const int N = g.N;
     const float alpha = p.alpha, beta = p.beta;
 
     // blocks this warp writes: [c_lo, c_hi), the same for all lanes
     int c_hi = CH;
-    while (c_hi > 0 && col_base + 32 * (c_hi - 1) >= N) --c_hi;
+    while (c_hi > 0 && col_base + EPI_COLS * (c_hi - 1) >= N) --c_hi;
     if (row_base >= g.M) c_hi = 0;  // every row of this warp is past the matrix
     int c_lo = 0;
-    if (MODE != MODE_UPDATE)
-        while (c_lo < c_hi && col_base + 32 * c_lo + 31 < row_base) ++c_lo;  // below the diagonal
+    while (c_lo < c_hi && col_base + EPI_COLS * c_lo < col_min) ++c_lo;
     const int nblocks = c_hi - c_lo;
 
     // Blocks are numbered across tiles (eb.seq) and block n uses slot
-    // n % RING (mirror slot 2 + n % 2).  Every block commits exactly one bulk
-    // group (possibly empty), so after block n's "at most RING-AHEAD groups
-    // still reading" every slot of blocks <= n-(RING-AHEAD) is free -- in
-    // particular the slot the addend load for block n+AHEAD overwrites, in
-    // this tile or at the start of the next one.
+    // n % NSLOT.  Every block commits exactly one bulk group, so after block
+    // n's "at most NSLOT - AHEAD groups still reading" every slot of blocks
+    // <= n - (NSLOT - AHEAD) is free -- in particular the slot the addend
+    // load for block n + AHEAD overwrites, in this tile or the next one.
     const uint32_t s0 = eb.seq;
     auto issue = [&](int k) {  // addend of the k-th written block of this tile
         if (MODE == MODE_SYRK) return;
-        const int b = static_cast<int>((s0 + k) % RING);
+        const int b = static_cast<int>((s0 + k) % NSLOT);
         if (lane == 0) {
             fence_proxy_async_smem();
             mbar_expect_tx(eb.bar[b], EBUF_BYTES);
-            tma_load_3d(eb.buf[b], &g.tm_e, col_base + 32 * (c_lo + k), row_base, tile.mat, eb.bar[b]);
+            tma_load_3d(eb.buf[b], &g.tm_e, col_base + EPI_COLS * (c_lo + k), row_base, tile.mat, eb.bar[b]);
         }
         eb.pending |= 1u << b;
     };
 #pragma unroll
-    for (int k = 0; k < AHEAD; ++k)
+    for (int k = 0; k < EPI_AHEAD; ++k)
         if (k < nblocks) issue(k);
 
     if (!wait_bounded(tfull, acc_phase, abort_flag, p.status)) return false;
     tc_fence_after();
     const uint32_t t_addr = t_acc + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int sw = (lane >> 1) & 3;  // 64-byte swizzle of this lane's row
+    // swizzle of this lane's row: 16-byte chunk q sits at q ^ sw
+    const int sw = EROW_BYTES == 64 ? (lane >> 1) & 3 : lane & 7;
 
     for (int k = 0; k < nblocks; ++k) {
         const int c = c_lo + k;
-        const int b = static_cast<int>((s0 + k) % RING);
-        const int mb = 2 + static_cast<int>((s0 + k) & 1);  // mirror slot (SYRK/POLY)
-        const int col0 = col_base + 32 * c;
+        const int b = static_cast<int>((s0 + k) % NSLOT);
         __syncwarp();
-        float v[32];
-        tmem_load_32cols(t_addr + static_cast<uint32_t>((half * CH + c) * 32), v);
-        uint8_t* brow = eb.ptr[b] + lane * 64;
-        uint4 e[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
-                      make_uint4(0u, 0u, 0u, 0u)};
+        uint8_t* brow = eb.ptr[b] + lane * EROW_BYTES;
         if (MODE != MODE_SYRK) {
             if (!wait_bounded(eb.bar[b], (eb.phase >> b) & 1u, abort_flag, p.status)) return false;
             eb.phase ^= 1u << b;
             eb.pending &= ~(1u << b);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) e[q] = *reinterpret_cast<const uint4*>(brow + ((q ^ sw) << 4));
         }
-        const bool diagonal = MODE != MODE_UPDATE && col0 == row_base;
-        if (!diagonal) {
+#pragma unroll
+        for (int h = 0; h < EPI_COLS / 32; ++h) {
+            float v[32];
+            tmem_load_32cols(t_addr + static_cast<uint32_t>((half * CH + c) * EPI_COLS + 32 * h), v);
+            uint4 e[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                          make_uint4(0u, 0u, 0u, 0u)};
+            if (MODE != MODE_SYRK) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    e[q] = *reinterpret_cast<const uint4*>(brow + (((4 * h + q) ^ sw) << 4));
+            }
             uint32_t w[16];
             chunk_values<MODE>(v, e, alpha, beta, w);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(brow + ((q ^ sw) << 4)) =
+                *reinterpret_cast<uint4*>(brow + (((4 * h + q) ^ sw) << 4)) =
                     make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-            if (MODE != MODE_UPDATE) {
-                // mirror block: element (col0 + j, row_base + lane) at j * 32 + lane
-                uint16_t* mrow = reinterpret_cast<uint16_t*>(eb.ptr[mb]);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    mrow[(2 * i) * 32 + lane] = static_cast<uint16_t>(w[i] & 0xffffu);
-                    mrow[(2 * i + 1) * 32 + lane] = static_cast<uint16_t>(w[i] >> 16);
-                }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_3d(&g.tm_d, eb.buf[b], col0, row_base, tile.mat);
-                if (MODE != MODE_UPDATE) tma_store_3d(&g.tm_m, eb.buf[mb], row_base, col0, tile.mat);
-            }
-        } else if (row < g.M) {
-            uint16_t* drow = D + static_cast<int64_t>(row) * g.ld;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int col = col0 + j;
-                if (col < N && col >= row) {
-                    float val = v[j];
-                    if (MODE == MODE_POLY) {
-                        const uint16_t ebits =
-                            *reinterpret_cast<const uint16_t*>(brow + (((j >> 3) ^ sw) << 4) + (j & 7) * 2);
-                        const float ev = __uint_as_float(static_cast<uint32_t>(ebits) << 16);
-                        val = __fadd_rn(__fmul_rn(alpha, ev), __fmul_rn(beta, val));
-                    }
-                    const uint16_t bv = to_bf16(val);
-                    drow[col] = bv;
-                    if (col > row) D[static_cast<int64_t>(col) * g.ld + row] = bv;
-                }
-            }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
         if (lane == 0) {
+            tma_store_3d(&g.tm_d, eb.buf[b], col_base + EPI_COLS * c, row_base, tile.mat);
             bulk_commit();
-            bulk_wait_read<RING - AHEAD>();
+            bulk_wait_read<NSLOT - EPI_AHEAD>();
         }
         __syncwarp();
-        if (k + AHEAD < nblocks) issue(k + AHEAD);
+        if (k + EPI_AHEAD < nblocks) issue(k + EPI_AHEAD);
     }
     eb.seq = s0 + static_cast<uint32_t>(nblocks);
     return true;
@@ -556,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             tma_prefetch_desc(&p.g[gi].tm_b);
             if (MODE != MODE_SYRK) tma_prefetch_desc(&p.g[gi].tm_e);
             tma_prefetch_desc(&p.g[gi].tm_d);
-            if (MODE != MODE_UPDATE) tma_prefetch_desc(&p.g[gi].tm_m);
+            if (MODE != MODE_SYRK) tma_prefetch_desc(&p.g[gi].tm_t);
         }
     }
     if (warp == 1) {
@@ -588,13 +594,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
                 const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
                 const uint32_t sb = sa + A_BYTES;
                 mbar_expect_tx(fb, STAGE_BYTES);
-                tma_load_3d(sa, &g.tm_a, kb * BK, tile.ti * BM, tile.mat, fb);
-                if (MODE == MODE_UPDATE) {
-#pragma unroll
-                    for (int q = 0; q < BN / 64; ++q)
-                        tma_load_3d(sb + q * (64 * BK * 2), &g.tm_b, tile.tj * BN + 64 * q, kb * BK, tile.mat, fb);
+                auto load3 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
+                    tma_load_3d(dst, map, c0, c1, c2, fb);
+                };
+                auto load4 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+                    tma_load_4d(dst, map, c0, c1, c2, c3, fb);
+                };
+                const bool chunked = g.chunked != 0;
+                // A operand: 128 rows of row block ti (POLY/UPDATE read the
+                // symmetric factor transposed left of the diagonal block)
+                if (MODE != MODE_SYRK && read_transposed(kb, tile.ti, 1))
+                    load_mn(sa, &g.tm_t, chunked, 2, tile.ti * BM, BM / 64, kb, tile.mat, load3, load4);
+                else
+                    tma_load_3d(sa, &g.tm_a, kb * BK, tile.ti * BM, tile.mat, fb);
+                // B operand: 256 rows = row blocks 2tj and 2tj+1; UPDATE reads X
+                // MN-major (4 chunks per copy), POLY each half per its own block
+                const int n0 = tile.tj * BN;
+                const bool t0 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj, 1));
+                const bool t1 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj + 1, 1));
+                if (MODE == MODE_UPDATE)
+                    load_mn(sb, &g.tm_b, chunked, 4, n0, BN / 64, kb, tile.mat, load3, load4);
+                else if (t0)
+                    load_mn(sb, &g.tm_t, chunked, 2, n0, BN / 64, kb, tile.mat, load3, load4);
+                else if (t1) {
+                    tma_load_3d(sb, &g.tm_a, kb * BK, n0, tile.mat, fb);  // 128 K-major rows
+                    load_mn(sb + A_BYTES, &g.tm_t, chunked, 2, n0 + BM, BM / 64, kb, tile.mat, load3, load4);
                 } else {
-                    tma_load_3d(sb, &g.tm_b, kb * BK, tile.tj * BN, tile.mat, fb);
+                    tma_load_3d(sb, &g.tm_b, kb * BK, n0, tile.mat, fb);
                 }
                 last_parity[stage] = static_cast<int>(phase);
                 if (++stage == STAGES) {
@@ -629,9 +655,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             if (MODE != MODE_UPDATE && (tile.ti & 1) && tile.tj == (tile.ti >> 1)) n_lo = BN / 2;
             const int rem = g.N - tile.tj * BN;
             if (rem < BN) n_hi = (rem + 15) & ~15;
-            const uint32_t idesc = instr_desc(BM, n_hi - n_lo, MODE == MODE_UPDATE);
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN + n_lo);
-            const uint32_t b_off = static_cast<uint32_t>(n_lo) * 128;  // K-major B rows are 128 bytes
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
             for (int kb = 0; kb < nk; ++kb) {
                 if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.status)) {
                     ok = false;
@@ -640,12 +664,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
                 tc_fence_after();
                 const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
                 const uint32_t sb = sa + A_BYTES;
+                // the same layout choices as the producer's
+                const bool ta = MODE != MODE_SYRK && read_transposed(kb, tile.ti, 1);
+                const bool t0 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj, 1));
+                const bool t1 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj + 1, 1));
+                // one MMA over [n_lo, n_hi), or one per half when the halves'
+                // layouts differ and both are computed
+                const bool split = t0 != t1 && n_lo < BN / 2 && n_hi > BN / 2;
+                const int seg_lo[2] = {n_lo, BN / 2};
+                const int seg_hi[2] = {split ? BN / 2 : n_hi, n_hi};
+                const bool seg_t[2] = {n_lo >= BN / 2 ? t1 : t0, t1};
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    const uint64_t adesc = smem_desc(sa + k * 32, 16, 1024);
-                    const uint64_t bdesc = (MODE == MODE_UPDATE) ? smem_desc(sb + k * 16 * 128, 64 * BK * 2, 1024)
-                                                                 : smem_desc(sb + b_off + k * 32, 16, 1024);
-                    tc_mma(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                for (int sg = 0; sg < 2; ++sg) {
+                    if (sg == 1 && !split) break;
+                    const uint32_t idesc = instr_desc(BM, seg_hi[sg] - seg_lo[sg], ta, seg_t[sg]);
+                    const uint32_t b_base = sb + static_cast<uint32_t>(seg_lo[sg]) * 128;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        tc_mma(d_tmem + static_cast<uint32_t>(seg_lo[sg]), operand_desc(sa, k, ta),
+                               operand_desc(b_base, k, seg_t[sg]), idesc, (kb | k) != 0 ? 1u : 0u);
                 }
                 tc_commit(smem_u32(&empty_bar[stage]));
                 if (++stage == STAGES) {
@@ -679,8 +716,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             const GroupParams& g = p.g[tile.group];
             const int acc = local & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
-            if (!epilogue_tile<MODE>(p, g, tile, tmem_base + static_cast<uint32_t>(acc * BN), quarter, half, lane,
-                                     smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, eb))
+            const int col_min = MODE == MODE_UPDATE ? 0 : tile.ti * BM;
+            if (!epilogue_tile<MODE>(p, g, tile, col_min, tmem_base + static_cast<uint32_t>(acc * BN), quarter, half,
+                                     lane, smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, eb))
                 break;
             tc_fence_before();
             __syncwarp();
@@ -752,6 +790,15 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar_cluster)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                  : "memory");
@@ -786,11 +833,13 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
 }
 
 // Columns of a pair tile the MMA computes: 256, or for the last column tile
-// of a ragged matrix the next multiple of 32 past the edge.  CTA r of the
+// of a ragged matrix the next multiple of 32 past the edge (of 128 with
+// chunked maps, so each CTA's half starts on a 64-row chunk).  CTA r of the
 // pair holds B columns [r * n / 2, (r + 1) * n / 2) of the tile.
-__device__ __forceinline__ int pair_tile_n(int N, int tj) {
-    const int rem = N - tj * BN;
-    return rem < BN ? ((rem + 31) & ~31) : BN;
+__device__ __forceinline__ int pair_tile_n(const GroupParams& g, int tj) {
+    const int rem = g.N - tj * BN;
+    const int q = g.chunked ? 127 : 31;
+    return rem < BN ? ((rem + q) & ~q) : BN;
 }
 
 template <int MODE>
@@ -866,7 +915,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             tma_prefetch_desc(&p.g[gi].tm_b);
             if (MODE != MODE_SYRK) tma_prefetch_desc(&p.g[gi].tm_e);
             tma_prefetch_desc(&p.g[gi].tm_d);
-            if (MODE != MODE_UPDATE) tma_prefetch_desc(&p.g[gi].tm_m);
+            if (MODE != MODE_SYRK) tma_prefetch_desc(&p.g[gi].tm_t);
         }
     }
     if (warp == 1) {
@@ -898,16 +947,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t fb_leader = mapa_shared(fb, 0);
                 const uint32_t sa = smem_u32(tiles + stage * PSTAGE_BYTES);
                 const uint32_t sb = sa + PA_BYTES;
-                const int b0 = tile.tj * BN + static_cast<int>(rank) * (pair_tile_n(g.N, tile.tj) / 2);
+                const int b0 = tile.tj * BN + static_cast<int>(rank) * (pair_tile_n(g, tile.tj) / 2);
                 if (rank == 0) mbar_expect_tx(fb, 2 * PSTAGE_BYTES);
-                tma_load_3d_pair(sa, &g.tm_a, kb * BK, tile.ti * BM, tile.mat, fb_leader);
-                if (MODE == MODE_UPDATE) {
-#pragma unroll
-                    for (int q = 0; q < BN / 2 / 64; ++q)
-                        tma_load_3d_pair(sb + q * (64 * BK * 2), &g.tm_b, b0 + 64 * q, kb * BK, tile.mat, fb_leader);
-                } else {
+                auto load3 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
+                    tma_load_3d_pair(dst, map, c0, c1, c2, fb_leader);
+                };
+                auto load4 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+                    tma_load_4d_pair(dst, map, c0, c1, c2, c3, fb_leader);
+                };
+                const bool chunked = g.chunked != 0;
+                // row blocks of 256 (the pair tile): both CTAs make the same choices
+                if (MODE != MODE_SYRK && read_transposed(kb, tile.ti >> 1, 2))
+                    load_mn(sa, &g.tm_t, chunked, 2, tile.ti * BM, BM / 64, kb, tile.mat, load3, load4);
+                else
+                    tma_load_3d_pair(sa, &g.tm_a, kb * BK, tile.ti * BM, tile.mat, fb_leader);
+                if (MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, tile.tj, 2)))
+                    load_mn(sb, MODE == MODE_UPDATE ? &g.tm_b : &g.tm_t, chunked, 2, b0, BN / 2 / 64, kb, tile.mat,
+                            load3, load4);
+                else
                     tma_load_3d_pair(sb, &g.tm_b, kb * BK, b0, tile.mat, fb_leader);
-                }
                 last_parity[stage] = static_cast<int>(phase);
                 if (++stage == PSTAGES) {
                     stage = 0;
@@ -933,7 +991,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
             if (!wait_bounded(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, abort_flag, p.status)) break;
             tc_fence_after();
-            const uint32_t idesc = instr_desc(2 * BM, pair_tile_n(g.N, tile.tj), MODE == MODE_UPDATE);
+            const int n = pair_tile_n(g, tile.tj);
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
             for (int kb = 0; kb < nk; ++kb) {
                 if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.status)) {
@@ -943,13 +1001,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t sa = smem_u32(tiles + stage * PSTAGE_BYTES);
                 const uint32_t sb = sa + PA_BYTES;
+                const bool ta = MODE != MODE_SYRK && read_transposed(kb, tile.ti >> 1, 2);
+                const bool tb = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, tile.tj, 2));
+                const uint32_t idesc = instr_desc(2 * BM, n, ta, tb);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    const uint64_t adesc = smem_desc(sa + k * 32, 16, 1024);
-                    const uint64_t bdesc = (MODE == MODE_UPDATE) ? smem_desc(sb + k * 16 * 128, 64 * BK * 2, 1024)
-                                                                 : smem_desc(sb + k * 32, 16, 1024);
-                    tc_mma_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
-                }
+                for (int k = 0; k < BK / 16; ++k)
+                    tc_mma_pair(d_tmem, operand_desc(sa, k, ta), operand_desc(sb, k, tb), idesc,
+                                (kb | k) != 0 ? 1u : 0u);
                 tc_commit_pair_mc(smem_u32(&empty_bar[stage]), 0x3);
                 if (++stage == PSTAGES) {
                     stage = 0;
@@ -982,8 +1040,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const GroupParams& g = p.g[tile.group];
             const int acc = local & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(local >> 1) & 1u;
-            if (!epilogue_tile<MODE>(p, g, tile, tmem_base + static_cast<uint32_t>(acc * BN), quarter, half, lane,
-                                     smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, eb))
+            // SYRK/POLY store the pair tile whole: its row block is 256 rows
+            const int col_min = MODE == MODE_UPDATE ? 0 : (tile.ti >> 1) * 2 * BM;
+            if (!epilogue_tile<MODE>(p, g, tile, col_min, tmem_base + static_cast<uint32_t>(acc * BN), quarter, half,
+                                     lane, smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, eb))
                 break;
             tc_fence_before();
             __syncwarp();
@@ -1044,6 +1104,35 @@ bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, i
     return r == CUDA_SUCCESS;
 }
 
+// 4-D chunked view of the same matrices for MN-major reads: dims {64,
+// rows, inner / 64, count} with strides {ld, 64 elements, matrix}, box {64,
+// box_rows, box_chunks}.  `inner` must be a multiple of 64 so no chunk
+// reaches past a row.
+bool make_map_chunked(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t count, int64_t ld,
+                      int64_t mat_stride, uint32_t box_rows, uint32_t box_chunks) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || inner % 64 != 0) return false;
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(inner / 64),
+                          static_cast<cuuint64_t>(count)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld * 2), 128, static_cast<cuuint64_t>(mat_stride)};
+    cuuint32_t box[4] = {64, box_rows, box_chunks, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// MN-major maps for a symmetric factor (2 chunks per copy) or X (UPDATE's
+// B operand, `x_chunks` per copy): chunked when the width allows it.
+bool make_mn_map(CUtensorMap* map, bool chunked, const void* base, int64_t inner, int64_t rows, int64_t count,
+                 int64_t ld, int64_t mat_stride, uint32_t chunks) {
+    return chunked ? make_map_chunked(map, base, inner, rows, count, ld, mat_stride, BK, chunks)
+                   : make_map(map, base, inner, rows, count, ld, mat_stride, 64, BK);
+}
+
+constexpr CUtensorMapSwizzle kEpiSwizzle = EROW_BYTES == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+
 int triangle_tiles(int tiles_m, int tiles_n) {
     int n = 0;
     for (int ti = 0; ti < tiles_m; ++ti) n += tiles_n - (ti >> 1);
@@ -1086,11 +1175,12 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, f
         GroupParams& g = prm.g[i];
         const uint16_t* X = G.X[cur];
         bool ok = true;
+        const bool chunked = G.mp % 64 == 0 && G.np % 64 == 0;
+        g.chunked = chunked ? 1 : 0;
         if (MODE == MODE_SYRK) {
             ok &= make_map(&g.tm_a, X, G.np, G.mp, G.count, G.ldx, G.x_stride, BK, BM);
             ok &= make_map(&g.tm_b, X, G.np, G.mp, G.count, G.ldx, G.x_stride, BK, kPair ? BN / 2 : BN);
-            ok &= make_map(&g.tm_d, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-            ok &= make_map(&g.tm_m, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+            ok &= make_map(&g.tm_d, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, EPI_COLS, 32, kEpiSwizzle);
             g.E = nullptr;
             g.D = G.A;
             g.ld = G.lda;
@@ -1101,9 +1191,9 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, f
         } else if (MODE == MODE_POLY) {
             ok &= make_map(&g.tm_a, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, BK, BM);
             ok &= make_map(&g.tm_b, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, BK, kPair ? BN / 2 : BN);
-            ok &= make_map(&g.tm_e, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-            ok &= make_map(&g.tm_d, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-            ok &= make_map(&g.tm_m, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
+            ok &= make_mn_map(&g.tm_t, chunked, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, 2);
+            ok &= make_map(&g.tm_e, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, EPI_COLS, 32, kEpiSwizzle);
+            ok &= make_map(&g.tm_d, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, EPI_COLS, 32, kEpiSwizzle);
             g.E = G.A;
             g.D = G.B;
             g.ld = G.lda;
@@ -1113,10 +1203,10 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, f
             g.K = static_cast<int32_t>(G.mp);
         } else {
             ok &= make_map(&g.tm_a, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, BK, BM);
-            ok &= make_map(&g.tm_b, X, G.np, G.mp, G.count, G.ldx, G.x_stride, 64, BK);
-            ok &= make_map(&g.tm_e, X, G.np, G.mp, G.count, G.ldx, G.x_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-            ok &= make_map(&g.tm_d, G.X[cur ^ 1], G.np, G.mp, G.count, G.ldx, G.x_stride, 32, 32,
-                           CU_TENSOR_MAP_SWIZZLE_64B);
+            ok &= make_mn_map(&g.tm_t, chunked, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, 2);
+            ok &= make_mn_map(&g.tm_b, chunked, X, G.np, G.mp, G.count, G.ldx, G.x_stride, kPair ? 2 : 4);
+            ok &= make_map(&g.tm_e, X, G.np, G.mp, G.count, G.ldx, G.x_stride, EPI_COLS, 32, kEpiSwizzle);
+            ok &= make_map(&g.tm_d, G.X[cur ^ 1], G.np, G.mp, G.count, G.ldx, G.x_stride, EPI_COLS, 32, kEpiSwizzle);
             g.E = X;
             g.D = G.X[cur ^ 1];
             g.ld = G.ldx;

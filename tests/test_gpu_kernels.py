@@ -79,7 +79,7 @@ def run_ns(shape, count, steps=5, coeffs=oracle.QUINTIC, seed=0, kind="gaussian"
 
 @pytest.mark.parametrize("coeffs,what", [((1.0, 0.0, 0.0), "identity"), ((0.0, 1.0, 0.0), "AX"),
                                          ((0.0, 0.0, 1.0), "AAX")])
-@pytest.mark.parametrize("shape", [(64, 64), (128, 256), (200, 328), (256, 512), (512, 900)])
+@pytest.mark.parametrize("shape", [(64, 64), (128, 256), (200, 328), (256, 512), (520, 1100), (512, 900)])
 def test_ns_single_stage_isolation(lib, shape, coeffs, what):
     """One step with one coefficient set isolates one product:
     (1,0,0) -> X;  (0,1,0) -> (X X^T) X;  (0,0,1) -> (X X^T)^2 X."""
@@ -92,11 +92,15 @@ def test_ns_single_stage_isolation(lib, shape, coeffs, what):
             assert rel_fro(got[i], ref) < NS_TOL, what
 
 
-# m' a multiple of 256 runs on CTA pairs (256x256 pair tiles), other m' on
-# single CTAs; both kinds, ragged edges included, are covered here.
+# m' within 1/16 of a multiple of 256 runs on CTA pairs (256x256 pair
+# tiles), other m' on single CTAs; both kinds, ragged edges included, are
+# covered here.  Symmetric factors are read transposed left of the diagonal
+# block: (520, 1100) has single-CTA tiles whose two 128-row halves of B take
+# different layouts in one k-block, (1000, 1100) pair tiles with a ragged
+# last row block.
 @pytest.mark.parametrize("shape", [(1, 1), (7, 13), (8, 8), (64, 64), (128, 256), (129, 257),
-                                   (200, 328), (256, 512), (300, 1000), (384, 384),
-                                   (512, 512), (512, 900), (768, 800)])
+                                   (200, 328), (256, 512), (300, 1000), (384, 384), (520, 1100),
+                                   (512, 512), (512, 900), (768, 800), (1000, 1100)])
 def test_ns_parity(lib, shape):
     count = 3 if shape[0] * shape[1] < 200_000 else 1
     X, got = run_ns(shape, count, seed=11)
