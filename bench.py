@@ -39,7 +39,7 @@ import workloads  # noqa: E402
 METRIC = "Muon optimizer-step ms & NS TFLOP/s (frac of BF16 peak); AdamW HBM GB/s"
 UNIT = "TFLOP/s"
 ADAMW_BYTES_PER_PARAM = 28  # read p, g, m, v (16 B), write p, m, v (12 B)
-KINDS = ("momentum_norm", "norm_finalize", "normalize_cast", "ns_syrk", "ns_poly", "ns_update",
+KINDS = ("momentum_norm", "norm_finalize", "x0_rescale", "ns_syrk", "ns_poly", "ns_update",
          "final_update", "adamw", "grad_guard")
 
 
@@ -84,12 +84,11 @@ def workload_flops(w: workloads.Workload, steps: int):
 
 def elementwise_bytes(w: workloads.Workload):
     """Algorithmic HBM bytes per step of the element-wise Muon stages."""
-    out = {"momentum_norm": 0, "normalize_cast": 0, "final_update": 0}
+    out = {"momentum_norm": 0, "final_update": 0}
     for s in w.matrices:
         n = s.rows * s.cols
         g = 2 if s.g_dtype.itemsize == 2 else 4
-        out["momentum_norm"] += n * (g + 4 + 4)        # read G, M; write M
-        out["normalize_cast"] += n * (g + 4 + 2)       # read G, M; write X0
+        out["momentum_norm"] += n * (g + 4 + 4 + 2)    # read G, M; write M, X0 = bf16(u)
         out["final_update"] += n * (4 + 2 + 4)         # read W, O; write W
     return out
 
@@ -408,7 +407,7 @@ def run_ours(args, rank, world, local_rank):
     for k in ns_kinds:
         s = stages[k]
         s["tflops"] = stage_flops[k] / (s["ms_per_step"] / 1e3) / 1e12
-    for k in ("momentum_norm", "normalize_cast", "final_update"):
+    for k in ("momentum_norm", "final_update"):
         if k in stages:
             stages[k]["gbs"] = ew_bytes[k] / (stages[k]["ms_per_step"] / 1e3) / 1e9
     d = stages[dominant]

@@ -136,8 +136,9 @@ muon_status_t muon_plan(const muon_matrix_t* mats, int64_t count,
  * `stream`.  For every matrix, with m' = min(rows, cols), n' = max:
  *   M  = mu M + (1-mu) G                       ([OPT] section 2.1)
  *   u  = (1-mu) G + mu M    (nesterov = 1; u = M when 0)
- *   X0 = bf16(u / (||u||_F + eps)), transposed to m' x n' when rows > cols
- *   ns_steps times:  A = X X^T;  B = b A + c A A;  X = a X + B X
+ *   X0 = bf16(u), transposed to m' x n' when rows > cols;  s = 1/(||u||_F + eps)
+ *   ns_steps times, starting from X = s X0 (s applied in fp32 inside the
+ *   first step, never stored):  A = X X^T;  B = b A + c A A;  X = a X + B X
  *                    (bf16 storage, fp32 accumulation; [OPT] section 4.2)
  *   W  = W - lr (wd W + rms_scale sqrt(n') O),  O = final X in W's layout
  *        (decoupled decay on the old W, [OPT] section 3.1; RMS matched to
@@ -219,7 +220,7 @@ muon_status_t muon_query_status(void* workspace, void* stream);
 typedef enum {
     MUON_KERNEL_MOMENTUM_NORM = 0,  /* momentum, look-ahead, sum of squares */
     MUON_KERNEL_NORM_FINALIZE = 1,  /* per-matrix norm scale                */
-    MUON_KERNEL_NORMALIZE_CAST = 2, /* X0 = bf16(u * s), wide orientation   */
+    MUON_KERNEL_X0_RESCALE = 2,     /* X0 rescale for out-of-range norms    */
     MUON_KERNEL_NS_SYRK = 3,        /* A = X X^T                            */
     MUON_KERNEL_NS_POLY = 4,        /* B = b A + c A A                      */
     MUON_KERNEL_NS_UPDATE = 5,      /* X = a X + B X                        */

@@ -41,7 +41,7 @@ EXPORTS = ("muon_workspace_bytes_per_matrix", "muon_workspace_size", "muon_plan"
            "muon_step_batched", "muon_newton_schulz", "adamw_step", "muon_query_status",
            "muon_status_string", "muon_version", "muon_launch_count", "muon_set_timing",
            "muon_timing_read", "muon_kernel_name", "muon_step_batched_noalloc")
-KERNEL_KINDS = ("momentum_norm", "norm_finalize", "normalize_cast", "ns_syrk", "ns_poly",
+KERNEL_KINDS = ("momentum_norm", "norm_finalize", "x0_rescale", "ns_syrk", "ns_poly",
                 "ns_update", "final_update", "adamw", "grad_guard")
 
 

@@ -23,7 +23,7 @@ using namespace muon;
 
 namespace {
 
-constexpr int32_t kVersion = 200;  // 0.2.0
+constexpr int32_t kVersion = 300;  // 0.3.0
 
 inline int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
 
@@ -181,12 +181,14 @@ muon_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MUON_OK : MUO
 // Lays out one chunk's shape groups in the workspace.
 struct ChunkLayout {
     std::vector<NsGroup> groups;
+    std::vector<int64_t> first;  // per group: its first plan row, counted from the chunk start
     std::vector<int64_t> x0_of;  // per plan row in chunk: X0 address offset
     std::vector<int64_t> x1_of;
 };
 
 void layout_groups(const std::vector<PlanRow>& plan, size_t b, size_t e, uint8_t* base, ChunkLayout& L) {
     L.groups.clear();
+    L.first.clear();
     L.x0_of.assign(e - b, 0);
     L.x1_of.assign(e - b, 0);
     uint8_t* cursor = base + (e - b) * kRecordBytes;
@@ -203,6 +205,8 @@ void layout_groups(const std::vector<PlanRow>& plan, size_t b, size_t e, uint8_t
         g.x_stride = round_up(2 * g.mp * g.ldx, 256);
         g.g_stride = round_up(2 * g.mp * g.lda, 256);
         g.count = c;
+        g.scale = nullptr;
+        g.scale_stride = 0;
         g.X[0] = reinterpret_cast<uint16_t*>(cursor);
         g.X[1] = reinterpret_cast<uint16_t*>(cursor + c * g.x_stride);
         g.A = reinterpret_cast<uint16_t*>(cursor + 2 * c * g.x_stride);
@@ -213,6 +217,7 @@ void layout_groups(const std::vector<PlanRow>& plan, size_t b, size_t e, uint8_t
         }
         cursor += 2 * c * g.x_stride + 2 * c * g.g_stride;
         L.groups.push_back(g);
+        L.first.push_back(static_cast<int64_t>(k - b));
         k = j;
     }
 }
@@ -313,7 +318,9 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
     ChunkLayout L;
     std::vector<MatDesc> descs;
     MatDesc* d_descs = reinterpret_cast<MatDesc*>(ws + kHeaderBytes);
-    int max_tiles = 1;
+    int max_tiles = 1;       // flat tiles, every matrix (gradient guard)
+    int max_wide_tiles = 0;  // flat tiles of the wide matrices (momentum pass)
+    int max_units = 0;       // tall-pass units (momentum pass)
     int64_t max_rows = 1, max_cols = 1;
 
     // Fills `descs` and the layout for plan rows [b, e) and uploads them.
@@ -324,6 +331,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
             ws + kHeaderBytes + round_up(static_cast<int64_t>(n) * static_cast<int64_t>(sizeof(MatDesc)), 256));
         descs.assign(n, MatDesc{});
         max_tiles = 1;
+        max_wide_tiles = max_units = 0;
         max_rows = max_cols = 1;
         for (int k = 0; k < n; ++k) {
             const PlanRow& row = plan[b + k];
@@ -353,9 +361,29 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
                       reinterpret_cast<uintptr_t>(m.M)) & 15u) == 0 ? 1 : 0;
             d.scale = 0.f;
             d.update_scale = update_scale(hp, m.rows, m.cols);
+            if (d.transposed) {
+                // units of tall_kc x tall_kr 64x64 tiles, at most kMaxNormTiles
+                const int64_t rt = (m.rows + 63) / 64, ct = (m.cols + 63) / 64;
+                const int64_t kc = (ct + kMaxNormTiles - 1) / kMaxNormTiles;
+                const int64_t cu = (ct + kc - 1) / kc;
+                const int64_t kr = (rt + kMaxNormTiles / cu - 1) / (kMaxNormTiles / cu);
+                d.tall_kc = static_cast<int32_t>(kc);
+                d.tall_kr = static_cast<int32_t>(kr);
+                d.nparts = static_cast<int32_t>(cu * ((rt + kr - 1) / kr));
+                max_units = std::max(max_units, d.nparts);
+            } else {
+                d.nparts = d.ntiles;
+                max_wide_tiles = std::max(max_wide_tiles, d.ntiles);
+            }
             max_tiles = std::max(max_tiles, d.ntiles);
             max_rows = std::max(max_rows, m.rows);
             max_cols = std::max(max_cols, m.cols);
+        }
+        // the first NS step applies each matrix's ns_scale, read from its record
+        for (size_t gi = 0; gi < L.groups.size(); ++gi) {
+            L.groups[gi].scale = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(d_descs + L.first[gi]) +
+                                                                offsetof(MatDesc, ns_scale));
+            L.groups[gi].scale_stride = static_cast<int64_t>(sizeof(MatDesc) / sizeof(float));
         }
         return from_cuda(cudaMemcpyAsync(d_descs, descs.data(), sizeof(MatDesc) * n, cudaMemcpyHostToDevice, st));
     };
@@ -391,11 +419,10 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
             s = prepare_chunk(b, e);
             if (s != MUON_OK) return s;
         }
-        s = from_cuda(launch_momentum_norm(d_descs, n, max_tiles, ms, st));
+        s = from_cuda(launch_momentum_norm(d_descs, n, max_wide_tiles, max_units, ms, st));
         if (s != MUON_OK) return s;
-        s = from_cuda(launch_norm_finalize(d_descs, n, hp->norm_eps, st));
-        if (s != MUON_OK) return s;
-        s = from_cuda(launch_normalize_cast(d_descs, n, max_rows, max_cols, ms, st));
+        // with no NS step X0 is the result, so it is normalised in place
+        s = from_cuda(launch_norm_finalize(d_descs, n, hp->norm_eps, hp->ns_steps == 0 ? 1 : 0, st));
         if (s != MUON_OK) return s;
         s = from_cuda(ns_run(L.groups.data(), static_cast<int>(L.groups.size()), hp->ns_steps, coeffs.data(),
                              &header->status, num_sms, st));
@@ -445,6 +472,8 @@ muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t 
         g.x_stride = round_up(2 * mp * g.ldx, 256);
         g.g_stride = round_up(2 * mp * g.lda, 256);
         g.count = cnt;
+        g.scale = nullptr;
+        g.scale_stride = 0;
         uint8_t* cursor = ws + cnt * static_cast<int64_t>(kRecordBytes);
         g.X[0] = reinterpret_cast<uint16_t*>(cursor);
         g.X[1] = reinterpret_cast<uint16_t*>(cursor + cnt * g.x_stride);

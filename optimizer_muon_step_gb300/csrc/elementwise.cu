@@ -1,9 +1,13 @@
 // Element-wise stages of the Muon step and the AdamW step (HBM-bound).
 //
-//   momentum_norm   M = mu M + (1-mu) G;  u = (1-mu) G + mu M;  per-tile sum u^2
-//   norm_finalize   s = 1 / (sqrt(sum u^2) + eps) per matrix (fp64 sum)
-//   normalize_cast  X0 = bf16(u * s) in the wide orientation (smem transpose
-//                   for tall matrices)
+//   momentum_norm   M = mu M + (1-mu) G;  u = (1-mu) G + mu M;  per-tile sum
+//                   u^2;  X0 = bf16(u) in the wide orientation (a tiled
+//                   shared-memory transpose for tall matrices)
+//   norm_finalize   s = 1 / (sqrt(sum u^2) + eps) per matrix (fp64 sum); the
+//                   first NS step applies s to X0 (s^2 to X0 X0^T), so the
+//                   normalised input s * bf16(u) is never stored; a matrix
+//                   whose norm lies outside [2^-40, 2^40] has a power of
+//                   two moved from s into X0 (exact)
 //   final_update    W = W - lr (wd W + scale O)
 //   grad guard      global sum of G^2 and non-finite count; clip factor
 //                   and skip decision
@@ -81,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
     __shared__ float red[kThreads / 32];
     const MatDesc& d = descs[blockIdx.y];
     const int tile = blockIdx.x;
-    if (tile >= d.ntiles) return;
+    if (d.transposed || tile >= d.ntiles) return;  // tall matrices: momentum_tall_kernel
     if (s.header && s.header->skip) return;  // the non-finite guard skips the step
     const float clip = s.scale_g ? s.header->clip : 1.f;
     const int64_t n = d.rows * d.cols;
@@ -90,6 +94,9 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
     float* __restrict__ M = d.M;
     const void* G = d.G;
     const int g_bf16 = d.g_bf16;
+    uint16_t* __restrict__ X0 = d.X0;
+    const int64_t cols = d.cols, ldx = d.ldx;
+    const bool x_flat = ldx == cols;  // X0 rows packed: X0 index = element index
     float acc = 0.f;
     int64_t scalar_from = start;
     if (d.vec) {
@@ -114,13 +121,22 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
             float4* mp = reinterpret_cast<float4*>(M + i);
             float4 m0 = mp[0], m1 = mp[1];
             float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            uint32_t xb[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 float u = momentum_elem(scaled_g(g[j], s.scale_g, clip), m[j], s);
                 acc = fmaf(u, u, acc);
+                xb[j] = f32_to_bf16(u);
             }
             mp[0] = make_float4(m[0], m[1], m[2], m[3]);
             mp[1] = make_float4(m[4], m[5], m[6], m[7]);
+            if (x_flat) {
+                *reinterpret_cast<uint4*>(X0 + i) = make_uint4(xb[0] | (xb[1] << 16), xb[2] | (xb[3] << 16),
+                                                               xb[4] | (xb[5] << 16), xb[6] | (xb[7] << 16));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) X0[((i + j) / cols) * ldx + (i + j) % cols] = static_cast<uint16_t>(xb[j]);
+            }
         }
         scalar_from = start + (nvec << 3);
     }
@@ -129,109 +145,177 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
         float u = momentum_elem(scaled_g(load_g(G, g_bf16, i), s.scale_g, clip), m, s);
         M[i] = m;
         acc = fmaf(u, u, acc);
+        X0[(i / cols) * ldx + i % cols] = f32_to_bf16(u);
     }
     float total = block_sum(acc, red);
     if (threadIdx.x == 0) d.partials[tile] = total;
 }
 
+// ---------------------------------------------------------------------------
+// Pass 1 for tall matrices (rows > cols, X0 = u^T): the same momentum step
+// over 64x64 tiles, bf16(u) staged in shared memory and written transposed.
+// A CTA ("unit") covers tall_kc column tiles x tall_kr row tiles and writes
+// one partial.  grid = (max units, matrices).
+// Thread (tx, ty) covers rows ty + 16 i (i < 4) and columns 4 tx .. 4 tx + 3.
+// ---------------------------------------------------------------------------
+// Six CTAs per SM (at most 40 registers a thread): at the unbounded 118
+// registers only two fit and the kernel ran at a third of HBM bandwidth.
+__global__ void __launch_bounds__(kThreads, 6) momentum_tall_kernel(const MatDesc* __restrict__ descs,
+                                                                 MomentumScalars s) {
+    __shared__ uint16_t tileT[kTile][kTile + 2];
+    __shared__ float red[kThreads / 32];
+    const MatDesc& d = descs[blockIdx.y];
+    const int unit = blockIdx.x;
+    if (!d.transposed || unit >= d.nparts) return;
+    if (s.header && s.header->skip) return;
+    const float clip = s.scale_g ? s.header->clip : 1.f;
+    const int64_t rows = d.rows, cols = d.cols;
+    const int64_t ctiles = (cols + kTile - 1) / kTile;
+    const int64_t cunits = (ctiles + d.tall_kc - 1) / d.tall_kc;
+    const int64_t ct_begin = (unit % cunits) * d.tall_kc;
+    const int64_t ct_end = min(ctiles, ct_begin + d.tall_kc);
+    const int64_t rt_begin = (unit / cunits) * d.tall_kr;
+    const int64_t rt_end = min((rows + kTile - 1) / kTile, rt_begin + d.tall_kr);
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float* __restrict__ M = d.M;
+    const void* G = d.G;
+    const int g_bf16 = d.g_bf16;
+    uint16_t* __restrict__ X0 = d.X0;
+    const int64_t ldx = d.ldx;
+    float acc = 0.f;
+    for (int64_t ct = ct_begin; ct < ct_end; ++ct) {
+        for (int64_t rt = rt_begin; rt < rt_end; ++rt) {
+            const int64_t r0 = rt * kTile, c0 = ct * kTile;
+            const bool full = d.vec && (cols % 4 == 0) && r0 + kTile <= rows && c0 + kTile <= cols;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rl = ty + 16 * i;
+                const int64_t r = r0 + rl;
+                const int64_t c = c0 + 4 * tx;
+                uint16_t b[4] = {0, 0, 0, 0};
+                if (full) {
+                    const int64_t off = r * cols + c;
+                    float4* mp = reinterpret_cast<float4*>(M + off);
+                    float4 m4 = *mp;
+                    float g[4];
+                    if (g_bf16) {
+                        uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(G) + off));
+                        g[0] = __uint_as_float(raw.x << 16); g[1] = __uint_as_float(raw.x & 0xffff0000u);
+                        g[2] = __uint_as_float(raw.y << 16); g[3] = __uint_as_float(raw.y & 0xffff0000u);
+                    } else {
+                        float4 g4 = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(G) + off));
+                        g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
+                    }
+                    float m[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float u = momentum_elem(scaled_g(g[j], s.scale_g, clip), m[j], s);
+                        acc = fmaf(u, u, acc);
+                        b[j] = f32_to_bf16(u);
+                    }
+                    *mp = make_float4(m[0], m[1], m[2], m[3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (r < rows && c + j < cols) {
+                            const int64_t off = r * cols + c + j;
+                            float m = M[off];
+                            const float u = momentum_elem(scaled_g(load_g(G, g_bf16, off), s.scale_g, clip), m, s);
+                            M[off] = m;
+                            acc = fmaf(u, u, acc);
+                            b[j] = f32_to_bf16(u);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tileT[4 * tx + j][rl] = b[j];
+            }
+            __syncthreads();
+            // X0 row = original column, X0 column = original row
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int cl = ty + 16 * i;
+                const int64_t xr = c0 + cl;
+                const int64_t xc = r0 + 4 * tx;
+                if (xr >= cols) continue;
+                if (full) {
+                    const uint2 packed =
+                        make_uint2(tileT[cl][4 * tx] | (static_cast<uint32_t>(tileT[cl][4 * tx + 1]) << 16),
+                                   tileT[cl][4 * tx + 2] | (static_cast<uint32_t>(tileT[cl][4 * tx + 3]) << 16));
+                    *reinterpret_cast<uint2*>(X0 + xr * ldx + xc) = packed;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (xc + j < rows) X0[xr * ldx + xc + j] = tileT[cl][4 * tx + j];
+                }
+            }
+            __syncthreads();
+        }
+    }
+    const float total = block_sum(acc, red);
+    if (threadIdx.x == 0) d.partials[unit] = total;
+}
+
+// Norms for which the first NS step applies the scale itself: products of
+// two bf16(u) elements of typical size ||u||^2 / (m n) stay far inside the
+// normal fp32 range for any matrix up to 2^31 elements.
+constexpr double kNormLo = 9.094947017729282e-13;  // 2^-40
+constexpr double kNormHi = 1.099511627776e12;      // 2^40
+
 // One warp per matrix: fp64 sum of the partials in a fixed order.
 __global__ void __launch_bounds__(kThreads) norm_finalize_kernel(MatDesc* __restrict__ descs,
-                                                                 int count, float eps) {
+                                                                 int count, float eps, int force_rescale) {
     const int k = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (k >= count) return;
     const MatDesc& d = descs[k];
     double s = 0.0;
-    for (int i = lane; i < d.ntiles; i += 32) s += static_cast<double>(d.partials[i]);
+    for (int i = lane; i < d.nparts; i += 32) s += static_cast<double>(d.partials[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) descs[k].scale = static_cast<float>(1.0 / (sqrt(s) + static_cast<double>(eps)));
-}
-
-// ---------------------------------------------------------------------------
-// Pass 2: X0 = bf16(u * s), written in the wide orientation.
-// grid = (col tiles, row tiles, matrices) over the caller's orientation.
-// Thread (tx, ty) covers rows ty + 16 i (i < 4) and columns 4 tx .. 4 tx + 3.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const MatDesc* __restrict__ descs,
-                                                                  MomentumScalars s) {
-    __shared__ uint16_t tileT[kTile][kTile + 2];
-    const MatDesc& d = descs[blockIdx.z];
-    const int64_t rows = d.rows, cols = d.cols;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTile;
-    if (r0 >= rows || c0 >= cols) return;
-    if (s.header && s.header->skip) return;
-    const float clip = s.scale_g ? s.header->clip : 1.f;
-    const float scale = d.scale;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const bool full = d.vec && (cols % 4 == 0) && r0 + kTile <= rows && c0 + kTile <= cols;
-    const float* __restrict__ M = d.M;
-    const void* G = d.G;
-    const int g_bf16 = d.g_bf16;
-    uint16_t* __restrict__ X0 = d.X0;
-    const int64_t ldx = d.ldx;
-    const bool tr = d.transposed != 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int rl = ty + 16 * i;
-        const int64_t r = r0 + rl;
-        const int64_t c = c0 + 4 * tx;
-        uint16_t b[4] = {0, 0, 0, 0};
-        if (full) {
-            const int64_t off = r * cols + c;
-            float4 m4 = *reinterpret_cast<const float4*>(M + off);
-            float g[4];
-            if (g_bf16) {
-                uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(G) + off);
-                g[0] = __uint_as_float(raw.x << 16); g[1] = __uint_as_float(raw.x & 0xffff0000u);
-                g[2] = __uint_as_float(raw.y << 16); g[3] = __uint_as_float(raw.y & 0xffff0000u);
-            } else {
-                float4 g4 = *reinterpret_cast<const float4*>(static_cast<const float*>(G) + off);
-                g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
-            }
-            const float m[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                b[j] = f32_to_bf16(__fmul_rn(lookahead_elem(scaled_g(g[j], s.scale_g, clip), m[j], s), scale));
-            if (!tr) {
-                uint2 packed = make_uint2(b[0] | (static_cast<uint32_t>(b[1]) << 16),
-                                          b[2] | (static_cast<uint32_t>(b[3]) << 16));
-                *reinterpret_cast<uint2*>(X0 + r * ldx + c) = packed;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (r < rows && c + j < cols) {
-                    const int64_t off = r * cols + c + j;
-                    b[j] = f32_to_bf16(__fmul_rn(
-                        lookahead_elem(scaled_g(load_g(G, g_bf16, off), s.scale_g, clip), M[off], s), scale));
-                    if (!tr) X0[r * ldx + c + j] = b[j];
-                }
-            }
-        }
-        if (tr) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tileT[4 * tx + j][rl] = b[j];
+    if (lane == 0) {
+        const double norm = sqrt(s);
+        const float scale = static_cast<float>(1.0 / (norm + static_cast<double>(eps)));
+        MatDesc& out = descs[k];
+        out.scale = scale;
+        out.rescaled = 0;
+        out.rescale_factor = 1.f;
+        out.ns_scale = scale;
+        if (force_rescale) {
+            out.rescaled = 1;
+            out.rescale_factor = scale;
+            out.ns_scale = 1.f;
+        } else if (norm > 0.0 && isfinite(norm) && (norm < kNormLo || norm > kNormHi)) {
+            // 2^k ||u|| in [0.5, 1): X0 elements stay at most 1 in size
+            int e = 0;
+            frexp(norm, &e);
+            out.rescaled = 1;
+            out.rescale_factor = ldexpf(1.f, -e);
+            out.ns_scale = ldexpf(scale, e);
         }
     }
-    if (!tr) return;
-    __syncthreads();
-    // transposed write: X0 row = original column, X0 column = original row
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int cl = ty + 16 * i;          // original column within tile
-        const int64_t xr = c0 + cl;          // X0 row
-        const int64_t xc = r0 + 4 * tx;      // X0 first column
-        if (xr >= cols) continue;
-        if (full) {
-            uint2 packed = make_uint2(tileT[cl][4 * tx] | (static_cast<uint32_t>(tileT[cl][4 * tx + 1]) << 16),
-                                      tileT[cl][4 * tx + 2] | (static_cast<uint32_t>(tileT[cl][4 * tx + 3]) << 16));
-            *reinterpret_cast<uint2*>(X0 + xr * ldx + xc) = packed;
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (xc + j < rows) X0[xr * ldx + xc + j] = tileT[cl][4 * tx + j];
+}
+
+// X0 = bf16(X0 * rescale_factor) for the matrices norm_finalize flagged.  A
+// fixed grid first scans the flags together, then walks the flagged matrices.
+constexpr int kRescaleCtas = 304;
+
+__global__ void __launch_bounds__(kThreads) x0_rescale_kernel(const MatDesc* __restrict__ descs, int count) {
+    int flagged = 0;
+    for (int k = threadIdx.x; k < count; k += kThreads) flagged |= descs[k].rescaled;
+    if (!__syncthreads_or(flagged)) return;  // the usual case: nothing to do
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int k = 0; k < count; ++k) {
+        const MatDesc& d = descs[k];
+        if (!d.rescaled) continue;
+        const float scale = d.rescale_factor;
+        const int64_t mp = d.transposed ? d.cols : d.rows;
+        const int64_t np = d.transposed ? d.rows : d.cols;
+        const int64_t ldx = d.ldx;
+        uint16_t* __restrict__ X0 = d.X0;
+        for (int64_t e = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; e < mp * np; e += stride) {
+            uint16_t* x = X0 + (e / np) * ldx + e % np;
+            *x = f32_to_bf16(__fmul_rn(bf16_to_f32(*x), scale));
         }
     }
 }
@@ -472,36 +556,34 @@ inline unsigned grid_for(int64_t work, int64_t per_block, int64_t cap) {
 
 }  // namespace
 
-cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles, MomentumScalars s,
+// max_tiles / max_units: largest ntiles over the wide matrices and nparts
+// over the tall ones (0 when there are none of that kind).
+cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles, int max_units, MomentumScalars s,
                                  cudaStream_t st) {
     for (int off = 0; off < count; off += 65535) {
         int n = count - off < 65535 ? count - off : 65535;
-        launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-        momentum_norm_kernel<<<dim3(max_tiles, n), kThreads, 0, st>>>(descs + off, s);
-        launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
+        if (max_tiles > 0) {
+            launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
+            momentum_norm_kernel<<<dim3(max_tiles, n), kThreads, 0, st>>>(descs + off, s);
+            launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
+        }
+        if (max_units > 0) {
+            launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
+            momentum_tall_kernel<<<dim3(max_units, n), kThreads, 0, st>>>(descs + off, s);
+            launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
+        }
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, cudaStream_t st) {
+cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, int force_rescale, cudaStream_t st) {
     const int per = kThreads / 32;
     launch_begin(MUON_KERNEL_NORM_FINALIZE, st);
-    norm_finalize_kernel<<<(count + per - 1) / per, kThreads, 0, st>>>(descs, count, eps);
+    norm_finalize_kernel<<<(count + per - 1) / per, kThreads, 0, st>>>(descs, count, eps, force_rescale);
     launch_end(MUON_KERNEL_NORM_FINALIZE, st);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_normalize_cast(const MatDesc* descs, int count, int64_t max_rows, int64_t max_cols,
-                                  MomentumScalars s, cudaStream_t st) {
-    const unsigned gx = static_cast<unsigned>((max_cols + kTile - 1) / kTile);
-    const unsigned gy = static_cast<unsigned>((max_rows + kTile - 1) / kTile);
-    if (gy > 65535u) return cudaErrorInvalidValue;
-    for (int off = 0; off < count; off += 65535) {
-        int n = count - off < 65535 ? count - off : 65535;
-        launch_begin(MUON_KERNEL_NORMALIZE_CAST, st);
-        normalize_cast_kernel<<<dim3(gx, gy, n), kThreads, 0, st>>>(descs + off, s);
-        launch_end(MUON_KERNEL_NORMALIZE_CAST, st);
-    }
+    launch_begin(MUON_KERNEL_X0_RESCALE, st);
+    x0_rescale_kernel<<<kRescaleCtas, kThreads, 0, st>>>(descs, count);
+    launch_end(MUON_KERNEL_X0_RESCALE, st);
     return cudaGetLastError();
 }
 

@@ -21,19 +21,29 @@ struct MatDesc {
     float* partials;     // per-tile sums of u^2 (kMaxNormTiles entries)
     int64_t rows, cols;  // caller's orientation
     int64_t ldx;         // row stride of X0 / O in elements
-    int64_t tile_len;    // elements per momentum tile (multiple of 8)
-    int32_t ntiles;      // momentum tiles
+    int64_t tile_len;    // elements per flat tile (multiple of 8): wide momentum pass, gradient guard
+    int32_t ntiles;      // flat tiles
     int32_t g_bf16;      // 1: G is bf16
     int32_t transposed;  // 1: rows > cols, X holds the transpose
     int32_t vec;         // 1: W, G, M are 16-byte aligned
     float scale;         // 1 / (||u||_F + eps), written by the finalize kernel
     float update_scale;  // rms_scale * sqrt(n')
+    int32_t nparts;      // partials the momentum pass writes (flat tiles, or tall units)
+    int32_t tall_kr;     // tall pass: 64-row tiles per unit
+    int32_t tall_kc;     // tall pass: 64-column tiles per unit
+    int32_t rescaled;    // 1: X0 is multiplied in place by rescale_factor before NS
+    float rescale_factor;
+    float ns_scale;      // factor the first NS step applies to X0
     int32_t pad_[2];
 };
 
 constexpr int kMaxNormTiles = 1024;
 constexpr size_t kRecordBytes = 8192;     // per matrix, see muon_step.h
 constexpr size_t kHeaderBytes = 256;
+// a matrix's record and partials fit its kRecordBytes (header and rounding
+// covered by the slack); the NS kernels index ns_scale in float strides
+static_assert(sizeof(MatDesc) + sizeof(float) * kMaxNormTiles + 512 <= kRecordBytes, "record overflow");
+static_assert(sizeof(MatDesc) % sizeof(float) == 0, "record stride");
 
 // Start of the workspace: status word and the gradient guard's results.
 struct WsHeader {
@@ -69,11 +79,18 @@ void launch_begin(int kind, cudaStream_t st);
 void launch_end(int kind, cudaStream_t st);
 
 // ---- element-wise kernels (elementwise.cu) --------------------------------
-cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles,
+// Momentum pass: M updated, X0 = bf16(u) in the wide orientation (tall
+// matrices through a tiled transpose), per-unit sums of u^2 into the
+// partials.  `max_units` bounds nparts over the tall matrices.
+cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles, int max_units,
                                  MomentumScalars s, cudaStream_t st);
-cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, cudaStream_t st);
-cudaError_t launch_normalize_cast(const MatDesc* descs, int count, int64_t max_rows,
-                                  int64_t max_cols, MomentumScalars s, cudaStream_t st);
+// Norm: scale = 1 / (||u|| + eps) per matrix; the first NS step applies
+// ns_scale to X0 = bf16(u).  Normally ns_scale = scale.  A norm outside the
+// range where products of bf16(u) elements stay normal fp32 numbers moves
+// a power of two 2^k from the scale into X0 (X0 *= 2^k, ns_scale = scale *
+// 2^-k: exact, the NS result is unchanged).  With `force_rescale` (no NS
+// step follows) X0 = bf16(X0 * scale) and ns_scale = 1.
+cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, int force_rescale, cudaStream_t st);
 cudaError_t launch_final_update(const MatDesc* descs, int count, int64_t max_rows,
                                 int64_t max_cols, UpdateScalars s, cudaStream_t st);
 cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n,
@@ -98,6 +115,11 @@ struct NsGroup {
     int64_t mp, np, ldx, lda;
     int64_t x_stride, g_stride;  // bytes
     int64_t count;
+    // Per-matrix factor the first step applies to X (X0 holds the scaled
+    // input divided by it): matrix k's factor at scale[k * scale_stride];
+    // null when X0 is the input as is.
+    const float* scale;
+    int64_t scale_stride;
 };
 
 constexpr int kNsMaxGroups = 4;

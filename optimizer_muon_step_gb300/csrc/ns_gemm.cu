@@ -94,6 +94,8 @@ struct GroupParams {
     CUtensorMap tm_d;      // output block store, box {EPI_COLS, 32}, swizzled over the row
     const uint16_t* E;     // epilogue addend (POLY: A, UPDATE: X)
     uint16_t* D;           // output
+    const float* scale;    // first step of SYRK/UPDATE: X = scale * X0 per matrix, else null
+    int64_t scale_stride;  // floats between consecutive matrices' scales
     int64_t ld;            // row stride of D and E, elements
     int64_t bs;            // matrix stride of D and E, elements
     int32_t M, N, K;
@@ -378,7 +380,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // ---------------------------------------------------------------------------
 
 // Chunk values packed as bf16 pairs, w[i] = columns (2i, 2i+1):
-//   SYRK  acc;   POLY  alpha*E + beta*acc;   UPDATE  alpha*E + acc
+//   SYRK  beta*acc;   POLY, UPDATE  alpha*E + beta*acc
+// (beta = 1 for SYRK and UPDATE except on the first step, where the
+// per-matrix input scale s gives SYRK beta = s^2 and UPDATE alpha = a s,
+// beta = s; multiplying by 1 is exact.)
 template <int MODE>
 __device__ __forceinline__ void chunk_values(const float (&v)[32], const uint4 (&e)[4], float alpha, float beta,
                                              uint32_t (&w)[16]) {
@@ -389,12 +394,12 @@ __device__ __forceinline__ void chunk_values(const float (&v)[32], const uint4 (
         for (int h = 0; h < 4; ++h) {
             const int i = q * 4 + h;
             float lo = v[2 * i], hi = v[2 * i + 1];
-            if (MODE == MODE_POLY) {
+            if (MODE == MODE_SYRK) {
+                lo = __fmul_rn(beta, lo);
+                hi = __fmul_rn(beta, hi);
+            } else {
                 lo = __fadd_rn(__fmul_rn(alpha, bf16_lo(ew[h])), __fmul_rn(beta, lo));
                 hi = __fadd_rn(__fmul_rn(alpha, bf16_hi(ew[h])), __fmul_rn(beta, hi));
-            } else if (MODE == MODE_UPDATE) {
-                lo = __fadd_rn(__fmul_rn(alpha, bf16_lo(ew[h])), lo);
-                hi = __fadd_rn(__fmul_rn(alpha, bf16_hi(ew[h])), hi);
             }
             w[i] = pack_bf16x2(lo, hi);
         }
@@ -442,7 +447,16 @@ __device__ __forceinline__ bool epilogue_tile(const NsParams& p, const GroupPara
     const int row_base = tile.ti * BM + quarter * 32;
     const int col_base = tile.tj * BN + half * CH * EPI_COLS;
     const int N = g.N;
-    const float alpha = p.alpha, beta = p.beta;
+    float alpha = p.alpha, beta = p.beta;
+    if (MODE != MODE_POLY && g.scale != nullptr) {
+        const float sc = g.scale[static_cast<int64_t>(tile.mat) * g.scale_stride];
+        if (MODE == MODE_SYRK) {
+            beta = __fmul_rn(sc, sc);
+        } else {
+            alpha = __fmul_rn(alpha, sc);
+            beta = sc;
+        }
+    }
 
     // blocks this warp writes: [c_lo, c_hi), the same for all lanes
     int c_hi = CH;
@@ -1142,8 +1156,8 @@ int triangle_tiles(int tiles_m, int tiles_n) {
 int triangle_pair_tiles(int tiles_n) { return tiles_n * (tiles_n + 1) / 2; }
 
 template <int MODE, bool kPair>
-cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, float b, float c, int* status,
-                         int num_sms, cudaStream_t st) {
+cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first, float a, float b, float c,
+                         int* status, int num_sms, cudaStream_t st) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_pairs = 0;
@@ -1216,6 +1230,8 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, float a, f
             g.K = static_cast<int32_t>(G.mp);
         }
         if (!ok) return cudaErrorInvalidValue;
+        g.scale = (first && MODE != MODE_POLY) ? G.scale : nullptr;
+        g.scale_stride = G.scale_stride;
         g.count = static_cast<int32_t>(G.count);
         g.tiles_n = (g.N + BN - 1) / BN;
         if (kPair) {
@@ -1269,15 +1285,15 @@ bool use_pairs(const NsGroup& g) {
 
 template <int MODE>
 cudaError_t run_stage(const NsGroup* pair_groups, int npair, const NsGroup* single_groups, int nsingle, int cur,
-                      float a, float b, float c, int* status, int num_sms, cudaStream_t st) {
+                      bool first, float a, float b, float c, int* status, int num_sms, cudaStream_t st) {
     for (int off = 0; off < npair; off += kNsMaxGroups) {
         const int n = npair - off < kNsMaxGroups ? npair - off : kNsMaxGroups;
-        cudaError_t e = launch_stage<MODE, true>(pair_groups + off, n, cur, a, b, c, status, num_sms, st);
+        cudaError_t e = launch_stage<MODE, true>(pair_groups + off, n, cur, first, a, b, c, status, num_sms, st);
         if (e != cudaSuccess) return e;
     }
     for (int off = 0; off < nsingle; off += kNsMaxGroups) {
         const int n = nsingle - off < kNsMaxGroups ? nsingle - off : kNsMaxGroups;
-        cudaError_t e = launch_stage<MODE, false>(single_groups + off, n, cur, a, b, c, status, num_sms, st);
+        cudaError_t e = launch_stage<MODE, false>(single_groups + off, n, cur, first, a, b, c, status, num_sms, st);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -1293,11 +1309,14 @@ cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, const float* c
     for (int s = 0; s < steps; ++s) {
         const int cur = s & 1;
         const float a = coeffs[3 * s], b = coeffs[3 * s + 1], c = coeffs[3 * s + 2];
-        cudaError_t e = run_stage<MODE_SYRK>(pairs.data(), np, singles.data(), ns, cur, a, b, c, status, num_sms, st);
+        const bool first = s == 0;
+        cudaError_t e =
+            run_stage<MODE_SYRK>(pairs.data(), np, singles.data(), ns, cur, first, a, b, c, status, num_sms, st);
         if (e == cudaSuccess)
-            e = run_stage<MODE_POLY>(pairs.data(), np, singles.data(), ns, cur, a, b, c, status, num_sms, st);
+            e = run_stage<MODE_POLY>(pairs.data(), np, singles.data(), ns, cur, first, a, b, c, status, num_sms, st);
         if (e == cudaSuccess)
-            e = run_stage<MODE_UPDATE>(pairs.data(), np, singles.data(), ns, cur, a, b, c, status, num_sms, st);
+            e = run_stage<MODE_UPDATE>(pairs.data(), np, singles.data(), ns, cur, first, a, b, c, status, num_sms,
+                                       st);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -106,7 +106,7 @@ const char* muon_kernel_name(int32_t kind) {
     switch (kind) {
         case MUON_KERNEL_MOMENTUM_NORM: return "momentum_norm";
         case MUON_KERNEL_NORM_FINALIZE: return "norm_finalize";
-        case MUON_KERNEL_NORMALIZE_CAST: return "normalize_cast";
+        case MUON_KERNEL_X0_RESCALE: return "x0_rescale";
         case MUON_KERNEL_NS_SYRK: return "ns_syrk";
         case MUON_KERNEL_NS_POLY: return "ns_poly";
         case MUON_KERNEL_NS_UPDATE: return "ns_update";

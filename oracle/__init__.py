@@ -97,6 +97,8 @@ def _load():
             lib.oracle_muon_step_matrix_scaled.restype = ctypes.c_int
             lib.oracle_newton_schulz_table.argtypes = [P, i64, i64, ctypes.c_int, P, ctypes.c_int]
             lib.oracle_newton_schulz_table.restype = ctypes.c_int
+            lib.oracle_newton_schulz_scaled.argtypes = [P, i64, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_float]
+            lib.oracle_newton_schulz_scaled.restype = ctypes.c_int
             lib.oracle_update_scale.argtypes = [i64, i64, ctypes.c_float, ctypes.c_int]
             lib.oracle_update_scale.restype = ctypes.c_float
             lib.oracle_adamw_step.argtypes = [P, P, P, P, i64, P, i64]
@@ -154,19 +156,20 @@ QUINTIC = (3.4445, -4.7750, 2.0315)
 CUBIC = (1.5, -0.5, 0.0)  # [OPT] section 4.2: X <- (3X - X X^T X) / 2
 
 
-def newton_schulz(X, steps=5, coeffs=QUINTIC, emulate_bf16=True) -> np.ndarray:
-    """Run the NS iteration on a wide matrix X (rows <= cols).
+def newton_schulz(X, steps=5, coeffs=QUINTIC, emulate_bf16=True, x_scale=1.0) -> np.ndarray:
+    """Run the NS iteration on the wide matrix x_scale * X (rows <= cols).
 
     coeffs: one (a, b, c) for every step, or a sequence of `steps` triples.
     emulate_bf16=True: X must hold bf16 values; A, B and each new X are
-    rounded to bf16 at the GPU's storage points.  emulate_bf16=False: pure
-    fp64, for the closed-form checks."""
+    rounded to bf16 at the GPU's storage points, and x_scale is applied in
+    fp32 inside the first step.  emulate_bf16=False: pure fp64, for the
+    closed-form checks."""
     X = np.array(X, dtype=np.float64, order="C", copy=True)
     if X.ndim != 2 or X.shape[0] > X.shape[1]:
         raise ValueError("newton_schulz expects a wide 2-D matrix")
     table = coeff_table(coeffs, steps)
-    rc = _load().oracle_newton_schulz_table(_ptr(X), X.shape[0], X.shape[1], int(steps),
-                                            _ptr(table), 1 if emulate_bf16 else 0)
+    rc = _load().oracle_newton_schulz_scaled(_ptr(X), X.shape[0], X.shape[1], int(steps),
+                                             _ptr(table), 1 if emulate_bf16 else 0, float(x_scale))
     if rc:
         raise RuntimeError(f"oracle_newton_schulz failed ({rc})")
     return X
@@ -259,7 +262,8 @@ def momentum(G, M, mu=0.95, nesterov=True):
 
 
 def normalize(u, eps=1e-7):
-    """Steps 3-4: returns (X0 wide as float values, s)."""
+    """Steps 3-4: returns (X0 = bf16(u) wide as float values, s); the
+    normalised NS input is s * X0, s applied inside the first NS step."""
     u = np.ascontiguousarray(u, dtype=np.float32)
     rows, cols = u.shape
     X0 = np.empty((min(rows, cols), max(rows, cols)), dtype=np.float64)

@@ -126,19 +126,30 @@ static void transpose_f64(const double* X, double* XT, int64_t R, int64_t C)
  * X <- (3X - X X^T X)/2, i.e. (a,b,c) = (1.5, -0.5, 0); the library's
  * default is the quintic (a,b,c) = (3.4445, -4.7750, 2.0315), 5 steps.
  *
- * X is rows x cols, row-major, overwritten with the result.
- * emulate_bf16 != 0: the GPU's storage points are reproduced: the input is
- *   taken as given (already bf16 values), and A, B and the new X are each
- *   rounded fp64 -> fp32 -> bf16 once per step; the two epilogues are fp32:
+ * X is rows x cols, row-major, overwritten with the result.  The iteration's
+ * input is x_scale * X: the scale is applied inside the first step (below),
+ * never to a stored X, so X keeps the values it was given (bf16 values when
+ * emulating).
+ * emulate_bf16 != 0: the GPU's storage points are reproduced: A, B and the
+ *   new X are each rounded fp64 -> fp32 -> bf16 once per step, and the
+ *   epilogues are fp32 with s = x_scale on the first step, s = 1 after:
+ *       A = bf16( fl32(fl32(s*s) * float(X X^T)) )
  *       B = bf16( fl32(b*A) + fl32(c*float(A A)) )
- *       X = bf16( fl32(a*X) + float(B X) )
+ *       X = bf16( fl32(fl32(a*s)*X) + fl32(s*float(B X)) )
+ *   (a factor of 1 is exact, so later steps are the plain iteration).  With
+ *   no steps the result is bf16( fl32(x_scale * X) ).
  * emulate_bf16 == 0: everything stays in fp64 (used to check the iteration
  *   against its singular-value closed form). */
-int oracle_newton_schulz_table(double* X, int64_t rows, int64_t cols, int steps,
-                               const float* coeffs, int emulate_bf16)
+int oracle_newton_schulz_scaled(double* X, int64_t rows, int64_t cols, int steps,
+                                const float* coeffs, int emulate_bf16, float x_scale)
 {
     if (rows <= 0 || cols <= 0 || steps < 0 || rows > cols || (steps > 0 && !coeffs))
         return 1;
+    if (steps == 0) {
+        for (int64_t i = 0; i < rows * cols; ++i)
+            X[i] = emulate_bf16 ? bf16_round(x_scale * (float)X[i]) : (double)x_scale * X[i];
+        return 0;
+    }
     double* XT = (double*)malloc(sizeof(double) * rows * cols);
     double* A = (double*)malloc(sizeof(double) * rows * rows);
     double* AA = (double*)malloc(sizeof(double) * rows * rows);
@@ -150,12 +161,18 @@ int oracle_newton_schulz_table(double* X, int64_t rows, int64_t cols, int steps,
     }
     for (int s = 0; s < steps; ++s) {
         const float a = coeffs[3 * s], b = coeffs[3 * s + 1], c = coeffs[3 * s + 2];
-        /* A = X X^T */
+        const float xs = s == 0 ? x_scale : 1.0f;  /* input scale, first step only */
+        /* A = (xs X)(xs X)^T */
         transpose_f64(X, XT, rows, cols);
         matmul_f64(X, XT, A, rows, cols, rows);
-        if (emulate_bf16)
+        if (emulate_bf16) {
+            const float xs2 = xs * xs;
             for (int64_t i = 0; i < rows * rows; ++i)
-                A[i] = bf16_round((float)A[i]);
+                A[i] = bf16_round(xs2 * (float)A[i]);
+        } else {
+            for (int64_t i = 0; i < rows * rows; ++i)
+                A[i] *= (double)xs * (double)xs;
+        }
         /* B = b A + c A A */
         matmul_f64(A, A, AA, rows, rows, rows);
         for (int64_t i = 0; i < rows * rows; ++i) {
@@ -167,19 +184,28 @@ int oracle_newton_schulz_table(double* X, int64_t rows, int64_t cols, int steps,
                 Bm[i] = (double)b * A[i] + (double)c * AA[i];
             }
         }
-        /* X = a X + B X */
+        /* X = a (xs X) + B (xs X) */
         matmul_f64(Bm, X, BX, rows, rows, cols);
+        const float axs = a * xs;
         for (int64_t i = 0; i < rows * cols; ++i) {
             if (emulate_bf16) {
-                float t1 = a * (float)X[i];
-                X[i] = bf16_round(t1 + (float)BX[i]);
+                float t1 = axs * (float)X[i];
+                float t2 = xs * (float)BX[i];
+                X[i] = bf16_round(t1 + t2);
             } else {
-                X[i] = (double)a * X[i] + BX[i];
+                X[i] = (double)a * (double)xs * X[i] + (double)xs * BX[i];
             }
         }
     }
     free(XT); free(A); free(AA); free(Bm); free(BX);
     return 0;
+}
+
+/* The iteration on X itself (input scale 1). */
+int oracle_newton_schulz_table(double* X, int64_t rows, int64_t cols, int steps,
+                               const float* coeffs, int emulate_bf16)
+{
+    return oracle_newton_schulz_scaled(X, rows, cols, steps, coeffs, emulate_bf16, 1.0f);
 }
 
 /* The same iteration with one coefficient triple for every step. */
@@ -248,8 +274,12 @@ void oracle_momentum(const float* G, float* M, float* u, int64_t n, float mu, in
 
 /* Steps 3-4: Frobenius normalisation and bf16 rounding.
  *  3. ||u||_F summed in fp64 in element order; s = float(1/(sqrt(sum u^2)+eps))
- *  4. X0 = bf16(fl(u*s)) written wide (min x max): transposed when rows > cols
- *     so that NS works on the smaller Gram matrix X X^T.
+ *  4. X0 = bf16(u) written wide (min x max): transposed when rows > cols so
+ *     that NS works on the smaller Gram matrix X X^T.
+ * The normalised NS input is s * X0: the pages say the iteration runs in
+ * bf16 on the normalised matrix but not where the cast falls; here the
+ * look-ahead is cast once and s is applied in fp32 inside the first NS step
+ * (oracle_newton_schulz_scaled), the GPU path's rounding points.
  * X0 is a (min x max) fp64 array of bf16 values.  Returns s. */
 float oracle_normalize(const float* u, int64_t rows, int64_t cols, float eps, double* X0)
 {
@@ -262,7 +292,7 @@ float oracle_normalize(const float* u, int64_t rows, int64_t cols, float eps, do
     const float s = (float)(1.0 / (sqrt(ss) + (double)eps));
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c) {
-            double x0 = bf16_round(u[r * cols + c] * s);
+            double x0 = bf16_round(u[r * cols + c]);
             if (transposed)
                 X0[c * np + r] = x0;
             else
@@ -318,7 +348,8 @@ void oracle_final_update(float* W, const float* O, int64_t rows, int64_t cols,
  *   G   gradient, fp32 values (a bf16 gradient is passed already widened:
  *       the widening is exact)
  *   M   fp32 momentum, updated in place
- *   X0  optional out: the normalised bf16 NS input (wide, float values)
+ *   X0  optional out: the bf16 look-ahead the NS input is s times (wide,
+ *       float values)
  *   O   optional out: the NS output (wide, float values)
  * Returns 0 on success. */
 int oracle_muon_step_matrix_scaled(float* W, const float* G, float* M,
@@ -340,13 +371,25 @@ int oracle_muon_step_matrix_scaled(float* W, const float* G, float* M,
         return 2;
     }
     oracle_momentum_scaled(G, M, u, n, hp->momentum, hp->nesterov, g_scale, scale_g);
-    oracle_normalize(u, rows, cols, hp->norm_eps, X);
+    const float s = oracle_normalize(u, rows, cols, hp->norm_eps, X);
     if (X0_out)
         for (int64_t i = 0; i < n; ++i)
             X0_out[i] = (float)X[i];
-    int rc = hp->ns_coeffs
-                 ? oracle_newton_schulz_table(X, mp, np, hp->ns_steps, hp->ns_coeffs, 1)
-                 : oracle_newton_schulz(X, mp, np, hp->ns_steps, hp->ns_a, hp->ns_b, hp->ns_c, 1);
+    float table[300];
+    const float* coeffs = hp->ns_coeffs;
+    if (!coeffs) {
+        if (hp->ns_steps < 0 || hp->ns_steps > 100) {
+            free(u); free(X); free(O);
+            return 11;
+        }
+        for (int k = 0; k < hp->ns_steps; ++k) {
+            table[3 * k] = hp->ns_a;
+            table[3 * k + 1] = hp->ns_b;
+            table[3 * k + 2] = hp->ns_c;
+        }
+        coeffs = table;
+    }
+    int rc = oracle_newton_schulz_scaled(X, mp, np, hp->ns_steps, coeffs, 1, s);
     if (rc) {
         free(u); free(X); free(O);
         return 10 + rc;

@@ -168,11 +168,12 @@ def test_step_mixed_shapes(lib, gdt):
 
 
 def test_step_mixed_dtypes_and_unaligned(lib):
-    shapes = [(96, 160), (160, 96), (33, 65)]
-    W, G, M = make_mats(shapes, [torch.float32, torch.bfloat16, torch.float32], seed=2)
-    # an unaligned view forces the scalar path for one matrix
-    base = torch.randn(33 * 65 + 1, device=DEV) * 0.02
-    W[2] = base[1:].view(33, 65)
+    shapes = [(96, 160), (160, 96), (33, 65), (65, 33)]
+    W, G, M = make_mats(shapes, [torch.float32, torch.bfloat16, torch.float32, torch.float32], seed=2)
+    # unaligned views force the scalar paths, for a wide and a tall matrix
+    for k in (2, 3):
+        base = torch.randn(33 * 65 + 1, device=DEV) * 0.02
+        W[k] = base[1:].view(*shapes[k])
     host = [(w.cpu().numpy(), g.float().cpu().numpy(), mm.cpu().numpy()) for w, g, mm in zip(W, G, M)]
     hp = m.MuonHparams()
     m.muon_step_batched(W, G, M, hp)
@@ -212,6 +213,54 @@ def test_step_zero_gradient_is_pure_decay(lib):
         got = w.cpu().numpy()
         assert np.array_equal(got, ref)
         assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("magnitude", [1e-16, 1e14])
+def test_step_extreme_gradient_scale(lib, magnitude):
+    """Norms far outside [2^-40, 2^40]: X0 is normalised in place before the
+    first NS step instead of inside it (products of unnormalised bf16
+    elements would leave the normal fp32 range)."""
+    shapes = [(128, 256), (384, 128)]
+    W, G, M = make_mats(shapes, [torch.float32] * 2, seed=8)
+    for g, mm in zip(G, M):
+        g.mul_(magnitude / 1e-2)
+        mm.mul_(magnitude / 1e-2)
+    host = [(w.cpu().numpy(), g.float().cpu().numpy(), mm.cpu().numpy()) for w, g, mm in zip(W, G, M)]
+    hp = m.MuonHparams()
+    m.muon_step_batched(W, G, M, hp)
+    for i, (w0, g0, m0) in enumerate(host):
+        check_step(w0, g0, m0, W[i].cpu().numpy(), M[i].cpu().numpy(), hp)
+
+
+@pytest.mark.parametrize("p2", [2.0 ** 50, 2.0 ** -50])
+def test_out_of_range_norm_path_is_exact(lib, p2):
+    """Scaling G and M by a power of two scales u, bf16(u) and the norm
+    exactly, so with norm_eps = 0 the NS input s * bf16(u) is unchanged.
+    The scaled norms lie outside [2^-40, 2^40], where X0 takes a power of two
+    from the scale; the update must still be bit-identical."""
+    shapes = [(128, 256), (384, 128)]
+    W, G, M = make_mats(shapes, [torch.float32] * 2, seed=10)
+    W2 = [w.clone() for w in W]
+    G2 = [g * p2 for g in G]
+    M2 = [x * p2 for x in M]
+    hp = m.MuonHparams(norm_eps=0.0)
+    m.muon_step_batched(W, G, M, hp)
+    m.muon_step_batched(W2, G2, M2, hp)
+    for a, b in zip(W, W2):
+        assert torch.equal(a, b)
+    for a, b in zip(M, M2):
+        assert torch.equal(a * p2, b)
+
+
+def test_step_without_ns_steps(lib):
+    """ns_steps = 0: the update is the normalised look-ahead itself."""
+    shapes = [(96, 160), (160, 96)]
+    W, G, M = make_mats(shapes, [torch.float32] * 2, seed=9)
+    host = [(w.cpu().numpy(), g.float().cpu().numpy(), mm.cpu().numpy()) for w, g, mm in zip(W, G, M)]
+    hp = m.MuonHparams(ns_steps=0)
+    m.muon_step_batched(W, G, M, hp)
+    for i, (w0, g0, m0) in enumerate(host):
+        check_step(w0, g0, m0, W[i].cpu().numpy(), M[i].cpu().numpy(), hp)
 
 
 @pytest.mark.parametrize("nesterov", [False, True])

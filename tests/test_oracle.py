@@ -87,6 +87,26 @@ def test_ns_zero_steps_is_identity():
     assert np.array_equal(oracle.newton_schulz(X, steps=0), X)
 
 
+def test_input_scale_enters_the_first_step_only():
+    """newton_schulz(X, x_scale=s) iterates on s * X: in fp64 it equals the
+    iteration on the pre-scaled input; emulating bf16 with a power-of-two s
+    (every fp32 product then scales exactly) it equals it bit for bit; with
+    no steps it is bf16(s * X)."""
+    X = oracle.bf16_round(rand_wide(16, 40, 11))
+    s = float(np.float32(0.37))  # the scale is an fp32 argument
+    a = oracle.newton_schulz(X, emulate_bf16=False, x_scale=s)
+    b = oracle.newton_schulz(s * X.astype(np.float64), emulate_bf16=False)
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-12
+    R = rand_wide(16, 40, 11)
+    for p2 in (2.0 ** -3, 2.0 ** 5):
+        Xp = oracle.bf16_round((R / (np.linalg.norm(R) * p2)).astype(np.float32))  # p2 * Xp has norm ~1
+        c = oracle.newton_schulz(Xp, x_scale=p2)
+        d = oracle.newton_schulz(oracle.bf16_round((p2 * Xp).astype(np.float32)))
+        assert np.all(np.isfinite(d)) and np.array_equal(c, d)
+    e = oracle.newton_schulz(X, steps=0, x_scale=s)
+    assert np.array_equal(e, oracle.bf16_round((np.float32(s) * X).astype(np.float32)))
+
+
 def test_quintic_band_on_random_input():
     """For singular values of the normalised input in [1.5e-3, 1] the
     5-fold quintic lands in the scalar map's image of that interval."""
@@ -176,8 +196,9 @@ def test_momentum_is_an_exponential_average():
     hp0 = oracle.MuonConfig(momentum=0.0)
     _, M2, X0, _ = oracle.muon_step_matrix(W, G, np.ones_like(G), hp0)
     assert np.array_equal(M2, G)
-    # mu = 0: X0 is bf16(G / ||G||) elementwise within half a bf16 ulp
-    ref = (G / np.linalg.norm(G.astype(np.float64))).astype(np.float64)
+    # mu = 0: the look-ahead is G itself, so X0 = bf16(G) (the NS input is
+    # X0 / ||G|| up to eps): within half a bf16 ulp of G
+    ref = G.astype(np.float64)
     assert np.all(np.abs(X0 - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
 
 
@@ -191,7 +212,7 @@ def test_nesterov_uses_updated_momentum():
     hp = oracle.MuonConfig(momentum=0.5)
     _, M1, X0, _ = oracle.muon_step_matrix(W, Z, M, hp)
     assert np.array_equal(M1, 0.5 * M)
-    ref = M / np.linalg.norm(M.astype(np.float64))
+    ref = 0.25 * M.astype(np.float64)  # u = mu * (mu * M), exact for mu = 0.5
     assert np.all(np.abs(X0 - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
     # g != 0: Nesterov direction is (1-mu) g + mu M_new, plain is M_new
     hpn = oracle.MuonConfig(momentum=0.5, nesterov=True)
@@ -201,14 +222,21 @@ def test_nesterov_uses_updated_momentum():
     Mnew = 0.5 * M.astype(np.float64) + 0.5 * G
     un = 0.5 * G + 0.5 * Mnew
     for X, u in ((Xn, un), (Xp, Mnew)):
+        # the normalised input X0 / ||u|| is the direction of u
         r = u / np.linalg.norm(u)
-        assert np.all(np.abs(X - r) <= np.abs(r) * 2.0 ** -8 + 1e-12)
+        assert np.all(np.abs(X / np.linalg.norm(u) - r) <= np.abs(r) * 2.0 ** -8 + 1e-12)
 
 
 def test_normalised_input_has_unit_norm():
+    """The NS input s * X0, with X0 = bf16(u) and s = 1 / (||u|| + eps), has
+    unit Frobenius norm to bf16 rounding; the step's X0 is that bf16(u)."""
     W, G, M = _inputs(48, 80, 3)
     _, _, X0, _ = oracle.muon_step_matrix(W, G, M)
-    assert abs(np.linalg.norm(X0.astype(np.float64)) - 1.0) < 2.0 ** -8
+    _, u = oracle.momentum(G, M, 0.95, True)
+    X0b, s = oracle.normalize(u)
+    assert np.array_equal(X0, X0b)
+    assert np.array_equal(X0b, oracle.bf16_round(u))
+    assert abs(np.linalg.norm(s * X0b.astype(np.float64)) - 1.0) < 2.0 ** -8
 
 
 def test_update_rms_matches_adamw_band():
@@ -241,7 +269,7 @@ def test_tall_matrix_equals_transposed_wide():
     W1, M1, X0a, Oa = oracle.muon_step_matrix(W, G, M)
     W2, M2, X0b, Ob = oracle.muon_step_matrix(W.T, G.T, M.T)
     assert np.array_equal(M1, M2.T)
-    assert np.allclose(X0a, X0b, rtol=0, atol=2.0 ** -14)
+    assert np.array_equal(X0a, X0b)
     assert np.linalg.norm(Oa - Ob) / np.linalg.norm(Ob) < 1e-2
     assert np.allclose(W1, W2.T, rtol=1e-5, atol=1e-7)
 
@@ -410,7 +438,7 @@ def test_stage_functions_compose_to_the_step():
     W1, M1, X0, O = oracle.muon_step_matrix(W, G, M, hp)
     M2, u = oracle.momentum(G, M, hp.momentum, hp.nesterov)
     X0b, s = oracle.normalize(u, hp.norm_eps)
-    Ob = oracle.newton_schulz(X0b, hp.ns_steps).astype(np.float32)
+    Ob = oracle.newton_schulz(X0b, hp.ns_steps, x_scale=s).astype(np.float32)
     W2 = oracle.final_update(W, Ob, hp.lr, hp.weight_decay, hp.rms_scale)
     assert np.array_equal(M1, M2) and np.array_equal(X0, X0b)
     assert np.array_equal(O, Ob) and np.array_equal(W1, W2)
