@@ -1273,14 +1273,19 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first
     return cudaGetLastError();
 }
 
-// A shape group runs on CTA pairs when its 256-row pair tiles waste at most
-// 1/16 of the rows (m' a multiple of 256, or large): pairs halve each SM's
+// Whether a shape group runs a stage on CTA pairs.  Pairs halve each SM's
 // operand traffic and deepen the pipeline (measured 2% faster on 2048-row
-// matrices, 11% on 7168-row ones), but a half-empty last pair row (m' =
-// 1408) costs more than that.
-bool use_pairs(const NsGroup& g) {
+// matrices, 11% on 7168-row ones), but waste the rows of a part-empty last
+// pair row.  UPDATE pays that waste in full and takes pairs only when it is
+// at most 1/16 of the rows; SYRK and POLY, whose diagonal tiles are partly
+// redundant anyway, still gain at 1/8 (m' = 1408, 9% waste: POLY 7% faster,
+// SYRK even, UPDATE 5% slower).  SYRK and POLY always agree, so A and B are
+// stored in the same band layout; a 256-row band holds every block a
+// single-CTA UPDATE reads, so a single-CTA UPDATE may follow pair-run SYRK
+// and POLY (the reverse never occurs: 1/16 <= 1/8).
+bool use_pairs(const NsGroup& g, int mode) {
     const int64_t padded = (g.mp + 2 * BM - 1) / (2 * BM) * (2 * BM);
-    return (padded - g.mp) * 16 <= g.mp;
+    return (padded - g.mp) * (mode == MODE_UPDATE ? 16 : 8) <= g.mp;
 }
 
 template <int MODE>
@@ -1303,20 +1308,26 @@ cudaError_t run_stage(const NsGroup* pair_groups, int npair, const NsGroup* sing
 
 cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, const float* coeffs, int* status, int num_sms,
                    cudaStream_t st) {
-    std::vector<NsGroup> pairs, singles;
-    for (int i = 0; i < ngroups; ++i) (use_pairs(groups[i]) ? pairs : singles).push_back(groups[i]);
-    const int np = static_cast<int>(pairs.size()), ns = static_cast<int>(singles.size());
+    // [0]: SYRK and POLY, [1]: UPDATE
+    std::vector<NsGroup> pairs[2], singles[2];
+    for (int i = 0; i < ngroups; ++i) {
+        (use_pairs(groups[i], MODE_SYRK) ? pairs[0] : singles[0]).push_back(groups[i]);
+        (use_pairs(groups[i], MODE_UPDATE) ? pairs[1] : singles[1]).push_back(groups[i]);
+    }
+    const int np0 = static_cast<int>(pairs[0].size()), ns0 = static_cast<int>(singles[0].size());
+    const int np1 = static_cast<int>(pairs[1].size()), ns1 = static_cast<int>(singles[1].size());
     for (int s = 0; s < steps; ++s) {
         const int cur = s & 1;
         const float a = coeffs[3 * s], b = coeffs[3 * s + 1], c = coeffs[3 * s + 2];
         const bool first = s == 0;
-        cudaError_t e =
-            run_stage<MODE_SYRK>(pairs.data(), np, singles.data(), ns, cur, first, a, b, c, status, num_sms, st);
+        cudaError_t e = run_stage<MODE_SYRK>(pairs[0].data(), np0, singles[0].data(), ns0, cur, first, a, b, c,
+                                             status, num_sms, st);
         if (e == cudaSuccess)
-            e = run_stage<MODE_POLY>(pairs.data(), np, singles.data(), ns, cur, first, a, b, c, status, num_sms, st);
+            e = run_stage<MODE_POLY>(pairs[0].data(), np0, singles[0].data(), ns0, cur, first, a, b, c, status,
+                                     num_sms, st);
         if (e == cudaSuccess)
-            e = run_stage<MODE_UPDATE>(pairs.data(), np, singles.data(), ns, cur, first, a, b, c, status, num_sms,
-                                       st);
+            e = run_stage<MODE_UPDATE>(pairs[1].data(), np1, singles[1].data(), ns1, cur, first, a, b, c, status,
+                                       num_sms, st);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
