@@ -209,6 +209,16 @@ muon_status_t adamw_step(float* p, const float* g, float* m, float* v,
                          int64_t n, const adamw_hparams_t* hp, int64_t step,
                          void* stream);
 
+/* Failure-detection self-check (no counterpart on the pages).  Enqueues on
+ * `stream` one thread that waits, through the same bounded mbarrier wait as
+ * the Newton-Schulz kernels, on a barrier nothing ever arrives on.  After
+ * `limit_us` microseconds (1 .. 10^7) the wait gives up: it records
+ * MUON_ERR_TIMEOUT in the status word of `workspace` (device, >= 256 bytes,
+ * 256-byte aligned; the word is cleared first) and the kernel returns, so
+ * the context stays usable.  Read the result with muon_query_status.
+ * Returns MUON_OK once the check is enqueued. */
+muon_status_t muon_check_bounded_wait(void* workspace, int64_t limit_us, void* stream);
+
 /* Synchronises `stream`, reads and clears the status word a step left in
  * `workspace`; returns MUON_OK or what was recorded (MUON_ERR_TIMEOUT,
  * MUON_STEP_SKIPPED). */

@@ -40,7 +40,8 @@ MUON_STEP_SKIPPED = 8
 EXPORTS = ("muon_workspace_bytes_per_matrix", "muon_workspace_size", "muon_plan",
            "muon_step_batched", "muon_newton_schulz", "adamw_step", "muon_query_status",
            "muon_status_string", "muon_version", "muon_launch_count", "muon_set_timing",
-           "muon_timing_read", "muon_kernel_name", "muon_step_batched_noalloc")
+           "muon_timing_read", "muon_kernel_name", "muon_step_batched_noalloc",
+           "muon_check_bounded_wait")
 KERNEL_KINDS = ("momentum_norm", "norm_finalize", "x0_rescale", "ns_syrk", "ns_poly",
                 "ns_update", "final_update", "adamw", "grad_guard")
 
@@ -163,6 +164,8 @@ def load_library(path: str = LIB_PATH):
         lib.adamw_step.restype = ctypes.c_int
         lib.muon_query_status.argtypes = [P, P]
         lib.muon_query_status.restype = ctypes.c_int
+        lib.muon_check_bounded_wait.argtypes = [P, i64, P]
+        lib.muon_check_bounded_wait.restype = ctypes.c_int
         lib.muon_status_string.argtypes = [ctypes.c_int]
         lib.muon_status_string.restype = ctypes.c_char_p
         lib.muon_version.argtypes = []
@@ -349,6 +352,14 @@ def muon_query_status(workspace, stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status:
     0, MUON_ERR_TIMEOUT (6) or MUON_STEP_SKIPPED (8)."""
     return int(load_library().muon_query_status(ctypes.c_void_p(workspace.data_ptr()), _stream(stream)))
+
+
+def muon_check_bounded_wait(workspace, limit_us: int = 20000, stream=None) -> None:
+    """Enqueues the failure-detection self-check: a bounded wait that nothing
+    satisfies runs out after limit_us and records MUON_ERR_TIMEOUT (6) in the
+    workspace status; read it with muon_query_status."""
+    _check(load_library().muon_check_bounded_wait(ctypes.c_void_p(workspace.data_ptr()), int(limit_us),
+                                                  _stream(stream)), "muon_check_bounded_wait")
 
 
 def version() -> int:

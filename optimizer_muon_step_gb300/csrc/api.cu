@@ -535,6 +535,19 @@ muon_status_t adamw_step(float* p, const float* g, float* m, float* v, int64_t n
     return from_cuda(launch_adamw(p, g, m, v, n, sc, num_sms, static_cast<cudaStream_t>(stream)));
 }
 
+muon_status_t muon_check_bounded_wait(void* workspace, int64_t limit_us, void* stream) {
+    if (!workspace || limit_us < 1 || limit_us > 10000000) return MUON_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_ERR_MISALIGNED;
+    int num_sms = 0;
+    muon_status_t s = device_info(&num_sms);
+    if (s != MUON_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WsHeader* header = static_cast<WsHeader*>(workspace);
+    s = from_cuda(cudaMemsetAsync(header, 0, sizeof(WsHeader), st));
+    if (s != MUON_OK) return s;
+    return from_cuda(launch_wait_probe(&header->status, static_cast<long long>(limit_us) * 1000, st));
+}
+
 muon_status_t muon_query_status(void* workspace, void* stream) {
     if (!workspace) return MUON_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -129,6 +129,10 @@ constexpr int kNsMaxGroups = 4;
 // bounded-wait timeout.  Returns a CUDA error or cudaSuccess; a tensor-map
 // encoding failure returns cudaErrorInvalidValue.
 // `coeffs` is host memory of 3 * steps floats, step s using coeffs[3s..3s+2].
+// Launches the failure-detection self-check: a bounded wait that runs out
+// after limit_ns and records MUON_ERR_TIMEOUT in *status.
+cudaError_t launch_wait_probe(int* status, long long limit_ns, cudaStream_t st);
+
 cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, const float* coeffs,
                    int* status, int num_sms, cudaStream_t st);
 

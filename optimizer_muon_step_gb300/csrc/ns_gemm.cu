@@ -156,14 +156,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // (another role timed out) or this wait itself ran past the limit, in which
 // case the abort flag and the global status word are set.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             int* status) {
+                                             int* status, unsigned long long limit_ns = kTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > kTimeoutNs) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicCAS(status, 0, static_cast<int>(MUON_ERR_TIMEOUT));
                 return false;
@@ -1080,6 +1080,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Failure-detection self-check: one thread waits, through the kernels' own
+// bounded wait, on an mbarrier nothing ever arrives on.  After limit_ns the
+// wait records MUON_ERR_TIMEOUT in *status and the kernel returns.
+// ---------------------------------------------------------------------------
+__global__ void bounded_wait_probe_kernel(int* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    wait_bounded(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1305,6 +1320,11 @@ cudaError_t run_stage(const NsGroup* pair_groups, int npair, const NsGroup* sing
 }
 
 }  // namespace
+
+cudaError_t launch_wait_probe(int* status, long long limit_ns, cudaStream_t st) {
+    bounded_wait_probe_kernel<<<1, 32, 0, st>>>(status, static_cast<unsigned long long>(limit_ns));
+    return cudaGetLastError();
+}
 
 cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, const float* coeffs, int* status, int num_sms,
                    cudaStream_t st) {

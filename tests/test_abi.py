@@ -186,6 +186,14 @@ def test_step_new_hparam_validation(built):
     assert built.muon_status_string(8) == b"step skipped by the non-finite gradient guard"
 
 
+def test_bounded_wait_check_validation(built):
+    P = ctypes.c_void_p
+    assert built.muon_check_bounded_wait(None, 1000, None) == 1
+    assert built.muon_check_bounded_wait(P(4096), 0, None) == 1
+    assert built.muon_check_bounded_wait(P(4096), 10 ** 8, None) == 1
+    assert built.muon_check_bounded_wait(P(4100), 1000, None) == 3
+
+
 def test_library_never_loads_the_oracle(built):
     # the product path has no reference to the oracle
     for path in ("optimizer_muon_step_gb300/__init__.py", "optimizer_muon_step_gb300/build.py"):

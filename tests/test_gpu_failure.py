@@ -1,0 +1,45 @@
+"""Failure detection on the GPU without a fault: every wait in the kernels
+is bounded, and a wait that runs out leaves a status the host reads while
+the context stays usable.  The self-check entry point makes one such wait
+run out (an mbarrier nothing arrives on) with a short limit."""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import optimizer_muon_step_gb300 as m
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(lib):
+    ws = m.allocate_workspace(1 << 22)
+    t0 = time.perf_counter()
+    m.muon_check_bounded_wait(ws, limit_us=20000)
+    assert m.muon_query_status(ws) == 6  # MUON_ERR_TIMEOUT
+    elapsed = time.perf_counter() - t0
+    assert 0.015 < elapsed < 5.0  # the wait ran its limit, then returned
+    # the status word was cleared by the query, and the context still runs a step
+    assert m.muon_query_status(ws) == 0
+    gen = torch.Generator(device=DEV).manual_seed(3)
+    W = [torch.randn(96, 160, device=DEV, generator=gen) * 0.02]
+    G = [torch.randn(96, 160, device=DEV, generator=gen) * 1e-2]
+    M = [torch.randn(96, 160, device=DEV, generator=gen) * 1e-2]
+    W0, G0, M0 = (x[0].cpu().numpy() for x in (W, G, M))
+    m.muon_step_batched(W, G, M, m.MuonHparams(), workspace=ws)
+    assert m.muon_query_status(ws) == 0
+    oW, oM, _, _ = oracle.muon_step_matrix(W0, G0, M0)
+    assert np.array_equal(M[0].cpu().numpy(), oM)
+    d = W[0].cpu().numpy().astype(np.float64) - W0
+    assert np.linalg.norm(d - (oW - W0)) / np.linalg.norm(oW - W0) < 1e-2
+
+
+def test_bounded_wait_argument_checks(lib):
+    ws = m.allocate_workspace(4096)
+    for bad in (0, -5, 10 ** 8):
+        with pytest.raises(m.MuonError):
+            m.muon_check_bounded_wait(ws, limit_us=bad)
