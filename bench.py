@@ -74,15 +74,64 @@ def ns_stage_flops(mp: int, np_: int):
             "ns_update": 2 * mp * mp * np_}      # B X
 
 
+def _ceil(a: int, b: int) -> int:
+    return (a + b - 1) // b
+
+
+def ns_stage_issued_flops(mp: int, np_: int):
+    """Flops the tensor cores are issued for one NS iteration on one matrix,
+    per stage: the kernels' tile enumeration, counting computed halves of
+    diagonal tiles, rows and columns padded past the matrix and K rounded
+    up to 64.  Mirrors the tile choices of the library's NS launch code:
+    128x256 single-CTA tiles or 256x256 CTA-pair tiles (SYRK/POLY on pairs
+    when 256-row pair tiles waste at most 1/8 of the rows, UPDATE at 1/16),
+    the last column tile rounded to 16 (single), 32 (pairs) or 128 (pairs on
+    64-aligned shapes)."""
+    pad = _ceil(mp, 256) * 256 - mp
+    chunked = mp % 64 == 0 and np_ % 64 == 0
+
+    def col_widths(n, pair):
+        q = (128 if chunked else 32) if pair else 16
+        out = []
+        for j in range(_ceil(n, 256)):
+            rem = n - 256 * j
+            out.append(256 if rem >= 256 else _ceil(rem, q) * q)
+        return out
+
+    def triangle(k):
+        if pad * 8 <= mp:  # pairs: tiles (I, J >= I) of 256 x n_J
+            w = col_widths(mp, True)
+            return sum(256 * w[j] * k for i in range(len(w)) for j in range(i, len(w)))
+        w = col_widths(mp, False)
+        total = 0
+        for ti in range(_ceil(mp, 128)):
+            for tj in range(ti // 2, len(w)):
+                lo = 128 if (ti % 2 == 1 and tj == ti // 2) else 0
+                total += 128 * (w[tj] - lo) * k
+        return total
+
+    k_x, k_g = _ceil(np_, 64) * 64, _ceil(mp, 64) * 64
+    if pad * 16 <= mp:
+        upd = _ceil(mp, 256) * 256 * sum(col_widths(np_, True)) * k_g
+    else:
+        upd = _ceil(mp, 128) * 128 * sum(col_widths(np_, False)) * k_g
+    return {"ns_syrk": 2 * triangle(k_x), "ns_poly": 2 * triangle(k_g), "ns_update": 2 * upd}
+
+
 def workload_flops(w: workloads.Workload, steps: int):
+    """(algorithmic flops per stage, dense-equivalent flops, issued flops per
+    stage) of `steps` NS iterations on every matrix of the workload."""
     per = {"ns_syrk": 0, "ns_poly": 0, "ns_update": 0}
+    issued = dict(per)
     dense = 0
     for s in w.matrices:
         mp, np_ = min(s.rows, s.cols), max(s.rows, s.cols)
         for k, v in ns_stage_flops(mp, np_).items():
             per[k] += steps * v
+        for k, v in ns_stage_issued_flops(mp, np_).items():
+            issued[k] += steps * v
         dense += steps * (4 * mp * mp * np_ + 2 * mp ** 3)
-    return per, dense
+    return per, dense, issued
 
 
 def elementwise_bytes(w: workloads.Workload):
@@ -357,7 +406,7 @@ def run_ours(args, rank, world, local_rank):
     steps_ns = hp.ns_steps
     tens = workloads.make_muon(w, device=dev)
     batch = m.MuonBatch(tens.W, tens.G, tens.M, budget_bytes=int(args.budget_gb * 2 ** 30))
-    stage_flops, dense_flops = workload_flops(w, steps_ns)
+    stage_flops, dense_flops, issued_flops = workload_flops(w, steps_ns)
     step_flops = sum(stage_flops.values())
     ew_bytes = elementwise_bytes(w)
 
@@ -431,6 +480,7 @@ def run_ours(args, rank, world, local_rank):
     for k in ns_kinds:
         s = stages[k]
         s["tflops"] = stage_flops[k] / (s["ms_per_step"] / 1e3) / 1e12
+        s["tflops_issued"] = issued_flops[k] / (s["ms_per_step"] / 1e3) / 1e12
     for k in ("momentum_norm", "final_update"):
         if k in stages:
             stages[k]["gbs"] = ew_bytes[k] / (stages[k]["ms_per_step"] / 1e3) / 1e9
@@ -455,8 +505,11 @@ def run_ours(args, rank, world, local_rank):
                     "peak_kind": f"HBM copy, {peaks['source']}",
                     "algorithmic_per_launch": per_launch, "ms_per_launch": ms_launch, "traffic": None}
     ns_ms = sum(stages[k]["ms_per_step"] for k in ns_kinds)
+    issued_total = sum(issued_flops.values())
     ns_summary = {"ms_per_step": ns_ms,
                   "tflops_algorithmic": step_flops / (ns_ms / 1e3) / 1e12,
+                  "tflops_issued": issued_total / (ns_ms / 1e3) / 1e12,
+                  "frac_of_peak_issued": issued_total / (ns_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
                   "tflops_dense_equivalent": dense_flops / (ns_ms / 1e3) / 1e12,
                   "frac_of_peak_algorithmic": step_flops / (ns_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
                   "frac_of_peak_dense_equivalent": dense_flops / (ns_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"]}
