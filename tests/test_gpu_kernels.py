@@ -98,10 +98,12 @@ def test_ns_single_stage_isolation(lib, shape, coeffs, what):
 # block: (520, 1100) has single-CTA tiles whose two 128-row halves of B take
 # different layouts in one k-block, (1000, 1100) pair tiles with a ragged
 # last row block, (960, 1100) pair-run SYRK/POLY followed by a single-CTA
-# UPDATE.
+# UPDATE; (512, 832) and (768, 960) pair tiles on 64-aligned shapes (chunked
+# MN-major copies) with a ragged last column tile.
 @pytest.mark.parametrize("shape", [(1, 1), (7, 13), (8, 8), (64, 64), (128, 256), (129, 257),
                                    (200, 328), (256, 512), (300, 1000), (384, 384), (520, 1100),
-                                   (512, 512), (512, 900), (768, 800), (960, 1100), (1000, 1100)])
+                                   (512, 512), (512, 832), (512, 900), (768, 800), (768, 960), (960, 1100),
+                                   (1000, 1100)])
 def test_ns_parity(lib, shape):
     count = 3 if shape[0] * shape[1] < 200_000 else 1
     X, got = run_ns(shape, count, seed=11)
