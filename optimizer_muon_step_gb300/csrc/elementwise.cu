@@ -27,7 +27,7 @@ namespace muon {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTile = 64;  // normalize / update tile edge
+constexpr int kTile = 64;  // tile edge of the tall momentum and the final-update kernels
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) {
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
@@ -77,7 +77,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 // ---------------------------------------------------------------------------
-// Pass 1: momentum, look-ahead, per-tile sum of squares.
+// Momentum pass, wide matrices (rows <= cols, X0 = u): momentum, look-ahead,
+// X0 = bf16(u) and a per-tile sum of squares.
 // grid = (max tiles, matrices); each CTA handles one contiguous tile.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* __restrict__ descs,
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
 }
 
 // ---------------------------------------------------------------------------
-// Pass 1 for tall matrices (rows > cols, X0 = u^T): the same momentum step
+// Momentum pass, tall matrices (rows > cols, X0 = u^T): the same step
 // over 64x64 tiles, bf16(u) staged in shared memory and written transposed.
 // A CTA ("unit") covers tall_kc column tiles x tall_kr row tiles and writes
 // one partial.  grid = (max units, matrices).

@@ -92,12 +92,8 @@ struct GroupParams {
     CUtensorMap tm_t;      // symmetric factor read MN-major (transposed position), 2 chunks per copy
     CUtensorMap tm_e;      // epilogue addend, box {EPI_COLS, 32}, swizzled over the row
     CUtensorMap tm_d;      // output block store, box {EPI_COLS, 32}, swizzled over the row
-    const uint16_t* E;     // epilogue addend (POLY: A, UPDATE: X)
-    uint16_t* D;           // output
     const float* scale;    // first step of SYRK/UPDATE: X = scale * X0 per matrix, else null
     int64_t scale_stride;  // floats between consecutive matrices' scales
-    int64_t ld;            // row stride of D and E, elements
-    int64_t bs;            // matrix stride of D and E, elements
     int32_t M, N, K;
     int32_t count;
     int32_t tiles_n;
@@ -408,8 +404,8 @@ __device__ __forceinline__ void chunk_values(const float (&v)[32], const uint4 (
 
 // Per-warp state of the epilogue's bulk copies; lives across tiles.  Each
 // epilogue warp owns a ring of NSLOT block buffers (32 rows x EPI_COLS,
-// swizzled over the row length: 64 or 128 bytes);
-// a slot takes a block's addend in and the finished block out.
+// swizzled over the row length: 64 or 128 bytes); a slot takes a block's
+// addend in and the finished block out.
 struct EpiBufs {
     uint32_t buf[NSLOT];    // shared::cta addresses
     uint8_t* ptr[NSLOT];    // the same buffers as generic pointers
@@ -428,7 +424,7 @@ constexpr int EPI_AHEAD = MUON_EPI_AHEAD;
 static_assert(EPI_AHEAD >= 1 && EPI_AHEAD <= NSLOT, "addend distance must fit the ring");
 
 // Waits for the accumulator, then writes the warp's share of the tile,
-// 32x32 blocks at a time:
+// blocks of 32 rows x EPI_COLS columns at a time:
 //   addend (POLY: A, UPDATE: X): bulk tensor load into a ring slot,
 //     requested EPI_AHEAD blocks ahead; the first ones before the
 //     accumulator wait so they overlap the main loop;
@@ -1210,10 +1206,6 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first
             ok &= make_map(&g.tm_a, X, G.np, G.mp, G.count, G.ldx, G.x_stride, BK, BM);
             ok &= make_map(&g.tm_b, X, G.np, G.mp, G.count, G.ldx, G.x_stride, BK, kPair ? BN / 2 : BN);
             ok &= make_map(&g.tm_d, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, EPI_COLS, 32, kEpiSwizzle);
-            g.E = nullptr;
-            g.D = G.A;
-            g.ld = G.lda;
-            g.bs = G.g_stride / 2;
             g.M = static_cast<int32_t>(G.mp);
             g.N = static_cast<int32_t>(G.mp);
             g.K = static_cast<int32_t>(G.np);
@@ -1223,10 +1215,6 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first
             ok &= make_mn_map(&g.tm_t, chunked, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, 2);
             ok &= make_map(&g.tm_e, G.A, G.mp, G.mp, G.count, G.lda, G.g_stride, EPI_COLS, 32, kEpiSwizzle);
             ok &= make_map(&g.tm_d, G.B, G.mp, G.mp, G.count, G.lda, G.g_stride, EPI_COLS, 32, kEpiSwizzle);
-            g.E = G.A;
-            g.D = G.B;
-            g.ld = G.lda;
-            g.bs = G.g_stride / 2;
             g.M = static_cast<int32_t>(G.mp);
             g.N = static_cast<int32_t>(G.mp);
             g.K = static_cast<int32_t>(G.mp);
@@ -1236,10 +1224,6 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first
             ok &= make_mn_map(&g.tm_b, chunked, X, G.np, G.mp, G.count, G.ldx, G.x_stride, kPair ? 2 : 4);
             ok &= make_map(&g.tm_e, X, G.np, G.mp, G.count, G.ldx, G.x_stride, EPI_COLS, 32, kEpiSwizzle);
             ok &= make_map(&g.tm_d, G.X[cur ^ 1], G.np, G.mp, G.count, G.ldx, G.x_stride, EPI_COLS, 32, kEpiSwizzle);
-            g.E = X;
-            g.D = G.X[cur ^ 1];
-            g.ld = G.ldx;
-            g.bs = G.x_stride / 2;
             g.M = static_cast<int32_t>(G.mp);
             g.N = static_cast<int32_t>(G.np);
             g.K = static_cast<int32_t>(G.mp);
