@@ -56,11 +56,6 @@ __device__ __forceinline__ float momentum_elem(float g, float& m, const Momentum
     return s.nesterov ? __fadd_rn(gterm, __fmul_rn(s.mu, mnew)) : mnew;
 }
 
-// Look-ahead recomputed from the already updated momentum.
-__device__ __forceinline__ float lookahead_elem(float g, float mnew, const MomentumScalars& s) {
-    return s.nesterov ? __fadd_rn(__fmul_rn(s.one_minus_mu, g), __fmul_rn(s.mu, mnew)) : mnew;
-}
-
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
