@@ -145,6 +145,29 @@ def elementwise_bytes(w: workloads.Workload):
     return out
 
 
+def input_bytes(w: workloads.Workload) -> int:
+    """Bytes of W, G and M over every matrix of the workload."""
+    return sum(s.rows * s.cols * (4 + s.g_dtype.itemsize + 4) for s in w.matrices)
+
+
+def l2_note(w: workloads.Workload) -> str:
+    b = input_bytes(w)
+    if b < 4 * L2_BYTES:
+        return f"inputs {b / 2**20:.1f} MB fit in L2: L2 flushed by a 512 MB write before each timed step"
+    return f"inputs {b / 2**30:.1f} GB exceed the 129 MB L2; no flush needed"
+
+
+def workload_config(w: workloads.Workload, steps_ns: int, world: int) -> dict:
+    """The config object of the JSON line (the same for both arms)."""
+    stage_flops, dense_flops, _ = workload_flops(w, steps_ns)
+    return {"workload": f"{w.name}: {w.description}", "matrices": len(w.matrices),
+            "muon_params": w.muon_params, "ns_steps": steps_ns,
+            "ns_flops_per_step_algorithmic": sum(stage_flops.values()),
+            "ns_flops_per_step_dense_equivalent": dense_flops,
+            "l2": l2_note(w),
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def reduce_max(x: float, world: int, device=None) -> float:
     """Max of a per-rank float over all ranks (identity on one rank)."""
     if world == 1:
@@ -300,7 +323,7 @@ def run_reference(args, rank):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{w.name}: {w.description}", "parallelism": "replicas"},
+            "config": workload_config(w, workloads.MUON_HPARAMS["ns_steps"], args.gpus),
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
@@ -423,12 +446,10 @@ def run_ours(args, rank, world, local_rank):
     if m.muon_query_status(batch.workspace) != 0:
         raise RuntimeError("device status set during warm-up")
     in_bytes = sum(t.numel() * t.element_size() for t in tens.storage)
+    assert in_bytes == input_bytes(w)
     flush = None
     if in_bytes < 4 * L2_BYTES:
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-        l2_note = f"inputs {in_bytes / 2**20:.1f} MB fit in L2: L2 flushed by a 512 MB write before each timed step"
-    else:
-        l2_note = f"inputs {in_bytes / 2**30:.1f} GB exceed the 129 MB L2; no flush needed"
 
     # ---- device-timed region ----
     clocks = ClockSampler(local_rank)
@@ -591,12 +612,7 @@ def run_ours(args, rank, world, local_rank):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": f"{w.name}: {w.description}", "matrices": len(w.matrices),
-                           "muon_params": w.muon_params, "ns_steps": steps_ns,
-                           "ns_flops_per_step_algorithmic": step_flops,
-                           "ns_flops_per_step_dense_equivalent": dense_flops,
-                           "l2": l2_note,
-                           "parallelism": "replicas" if world > 1 else "single"},
+                "config": workload_config(w, steps_ns, world),
                 "roofline": roofline, "ns": ns_summary, "stages": stages, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": launches, "clocks": clk, "adamw": adamw, "guarded_step": guard}
         print(json.dumps(line), flush=True)
