@@ -276,35 +276,45 @@ class ClockSampler:
 # the CPU oracle (baseline and reference arm)
 # --------------------------------------------------------------------------
 
-ORACLE_BUDGET_FLOPS = 1.5e12  # about 20 s of the oracle on 16 cores (dense fp64 flops)
+# Dense fp64 flops of oracle work per sample.  The oracle runs at about 0.11
+# TFLOP/s (dense) on 16 host cores: the reference arm's per-step sample is
+# about 2 s, the cpu_baseline sample about 13 s.
+REFERENCE_STEP_FLOPS = 2.6e11
+CPU_BASELINE_FLOPS = 1.5e12
 
 
-def oracle_sample(w: workloads.Workload):
-    """A bounded sample of the workload for the CPU oracle: one matrix of its
-    most common shape, drawn from the workload's distributions, with as
-    many of the 5 NS iterations as fit about 20 s of oracle time (the
-    oracle multiplies full, not triangular, matrices)."""
+def oracle_sample(w: workloads.Workload, budget_flops: float):
+    """A bounded sample of the workload for the CPU oracle: matrices of its
+    most common shape, drawn from the workload's distributions, as many as
+    fit `budget_flops` (at least one), with as many of the 5 NS iterations
+    as fit when one matrix alone exceeds it (the oracle multiplies full, not
+    triangular, matrices)."""
     import collections
     shapes = collections.Counter((s.rows, s.cols) for s in w.matrices)
-    (rows, cols), _ = shapes.most_common(1)[0]
-    idx = next(i for i, s in enumerate(w.matrices) if (s.rows, s.cols) == (rows, cols))
-    t = workloads.make_muon(w, device="cpu", indices=[idx])
+    (rows, cols), count = shapes.most_common(1)[0]
     mp, np_ = min(rows, cols), max(rows, cols)
     dense_per_iter = 4 * mp * mp * np_ + 2 * mp ** 3
-    steps = max(1, min(workloads.MUON_HPARAMS["ns_steps"], int(ORACLE_BUDGET_FLOPS // dense_per_iter)))
-    flops = sum(ns_stage_flops(mp, np_).values()) * steps
-    desc = f"1 matrix {rows}x{cols}, {steps} of 5 NS iterations"
-    return (t.W[0].numpy(), t.G[0].float().numpy(), t.M[0].numpy()), flops, desc, steps
+    full = workloads.MUON_HPARAMS["ns_steps"]
+    steps = max(1, min(full, int(budget_flops // dense_per_iter)))
+    n_mats = max(1, min(count, int(budget_flops // (dense_per_iter * full)))) if steps == full else 1
+    idx = [i for i, s in enumerate(w.matrices) if (s.rows, s.cols) == (rows, cols)][:n_mats]
+    t = workloads.make_muon(w, device="cpu", indices=idx)
+    mats = [(t.W[k].numpy(), t.G[k].float().numpy(), t.M[k].numpy()) for k in range(len(idx))]
+    flops = sum(ns_stage_flops(mp, np_).values()) * steps * len(idx)
+    desc = f"{len(idx)} matri{'x' if len(idx) == 1 else 'ces'} {rows}x{cols}, {steps} of {full} NS iterations"
+    return mats, flops, desc, steps
 
 
-def time_oracle(w: workloads.Workload, repeats: int = 1):
+def time_oracle(w: workloads.Workload, budget_flops: float, repeats: int = 1):
+    """Wall times of `repeats` oracle steps over one bounded sample."""
     import oracle
-    (W, G, M), flops, desc, steps = oracle_sample(w)
+    mats, flops, desc, steps = oracle_sample(w, budget_flops)
     cfg = oracle.MuonConfig(**dict(workloads.MUON_HPARAMS, ns_steps=steps))
     times = []
     for _ in range(repeats):
         t0 = time.perf_counter()
-        oracle.muon_step_matrix(W, G, M, cfg)
+        for W, G, M in mats:
+            oracle.muon_step_matrix(W, G, M, cfg)
         times.append(time.perf_counter() - t0)
     return times, flops, desc, oracle.num_threads()
 
@@ -313,10 +323,10 @@ def run_reference(args, rank):
     if rank != 0:
         return
     w = workloads.get(args.workload)
-    _, _, _, cores = time_oracle(workloads.get("c1"))  # build + warm the library
+    time_oracle(workloads.get("c1"), REFERENCE_STEP_FLOPS)  # build + warm the library
     for _ in range(args.warmup):
-        time_oracle(w)
-    times, flops, desc, cores = time_oracle(w, repeats=args.steps)
+        time_oracle(w, REFERENCE_STEP_FLOPS)
+    times, flops, desc, cores = time_oracle(w, REFERENCE_STEP_FLOPS, repeats=args.steps)
     total = sum(times)
     value = flops * len(times) / total / 1e12
     sample = f"{desc}, of {len(w.matrices)} matrices, per step (full Muon step otherwise)"
@@ -603,7 +613,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- CPU oracle baseline (rank 0, one GPU only) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        times, flops, desc, cores = time_oracle(w, repeats=1)
+        times, flops, desc, cores = time_oracle(w, CPU_BASELINE_FLOPS, repeats=1)
         cpu = {"value": flops / times[0] / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{desc}, of {len(w.matrices)} matrices (full Muon step otherwise), "
                          f"{times[0]:.1f} s"}
