@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--no-guard", action="store_true")
     ap.add_argument("--subset", type=int, default=0,
                     help="profiling only: keep the first N matrices of the workload")
+    ap.add_argument("--adamw-params", type=int, default=0,
+                    help="profiling only: N parameters per AdamW buffer instead of the full embedding size")
     return ap.parse_args()
 
 
@@ -582,8 +584,8 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_adamw:
         c5 = workloads.get("c5")
         ahp = m.AdamwHparams(**workloads.ADAMW_HPARAMS)
-        bufs = [workloads.make_adamw(r * c, seed=c5.seed + i, device=dev)
-                for i, (r, c) in enumerate(c5.adamw_shapes)]
+        sizes = [args.adamw_params or r * c for r, c in c5.adamw_shapes]
+        bufs = [workloads.make_adamw(n, seed=c5.seed + i, device=dev) for i, n in enumerate(sizes)]
         n_params = sum(b.p.numel() for b in bufs)
         for _ in range(args.warmup):
             for b in bufs:
@@ -603,7 +605,9 @@ def run_ours(args, rank, world, local_rank):
         gbs = ADAMW_BYTES_PER_PARAM * n_params / (a_ms / 1e3) / 1e9
         k_ms = at[0] / at[1]
         k_gbs = ADAMW_BYTES_PER_PARAM * (n_params / len(bufs)) / (k_ms / 1e3) / 1e9
-        adamw = {"workload": "c5 AdamW: embedding + LM head, 2 x 163840x7168 fp32, t=100",
+        a_desc = ("c5 AdamW: embedding + LM head, 2 x 163840x7168 fp32, t=100" if not args.adamw_params else
+                  f"AdamW on 2 x {args.adamw_params} fp32 parameters (profiling size), t=100")
+        adamw = {"workload": a_desc,
                  "params": n_params, "ms_per_step": a_ms, "gbs": gbs,
                  "frac_of_hbm": gbs / peaks["hbm_gbs"], "frac_of_nominal_8tbs": gbs / 8000.0,
                  "kernel_ms_per_launch": k_ms, "kernel_gbs": k_gbs,
