@@ -321,6 +321,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
     int max_tiles = 1;       // flat tiles, every matrix (gradient guard)
     int max_wide_tiles = 0;  // flat tiles of the wide matrices (momentum pass)
     int max_units = 0;       // tall-pass units (momentum pass)
+    int tall_units[2] = {0, 0};  // the same, over tall matrices with fp32 / bf16 gradients
     int64_t max_rows = 1, max_cols = 1;
 
     // Fills `descs` and the layout for plan rows [b, e) and uploads them.
@@ -332,6 +333,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
         descs.assign(n, MatDesc{});
         max_tiles = 1;
         max_wide_tiles = max_units = 0;
+        tall_units[0] = tall_units[1] = 0;
         max_rows = max_cols = 1;
         for (int k = 0; k < n; ++k) {
             const PlanRow& row = plan[b + k];
@@ -371,6 +373,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
                 d.tall_kr = static_cast<int32_t>(kr);
                 d.nparts = static_cast<int32_t>(cu * ((rt + kr - 1) / kr));
                 max_units = std::max(max_units, d.nparts);
+                tall_units[d.g_bf16] = std::max(tall_units[d.g_bf16], d.nparts);
             } else {
                 d.nparts = d.ntiles;
                 max_wide_tiles = std::max(max_wide_tiles, d.ntiles);
@@ -419,7 +422,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
             s = prepare_chunk(b, e);
             if (s != MUON_OK) return s;
         }
-        s = from_cuda(launch_momentum_norm(d_descs, n, max_wide_tiles, max_units, ms, st));
+        s = from_cuda(launch_momentum_norm(d_descs, n, max_wide_tiles, tall_units[1], tall_units[0], ms, st));
         if (s != MUON_OK) return s;
         // with no NS step X0 is the result, so it is normalised in place
         s = from_cuda(launch_norm_finalize(d_descs, n, hp->norm_eps, hp->ns_steps == 0 ? 1 : 0, st));

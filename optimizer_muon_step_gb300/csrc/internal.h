@@ -81,8 +81,9 @@ void launch_end(int kind, cudaStream_t st);
 // ---- element-wise kernels (elementwise.cu) --------------------------------
 // Momentum pass: M updated, X0 = bf16(u) in the wide orientation (tall
 // matrices through a tiled transpose), per-unit sums of u^2 into the
-// partials.  `max_units` bounds nparts over the tall matrices.
-cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles, int max_units,
+// partials.  `tall_bf16` / `tall_f32` bound nparts over the tall matrices
+// with bf16 / fp32 gradients.
+cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles, int tall_bf16, int tall_f32,
                                  MomentumScalars s, cudaStream_t st);
 // Norm: scale = 1 / (||u|| + eps) per matrix; the first NS step applies
 // ns_scale to X0 = bf16(u).  Normally ns_scale = scale.  A norm outside the
