@@ -29,7 +29,7 @@ def _rank_main(rank, world, port, out):
 def test_two_rank_aggregation():
     world = 2
     port = 29500 + os.getpid() % 1000
-    with mp.Manager() as manager:
+    with mp.get_context("spawn").Manager() as manager:  # no fork of a process holding OpenMP threads
         out = manager.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
