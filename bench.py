@@ -85,8 +85,8 @@ def ns_stage_issued_flops(mp: int, np_: int):
     per stage: the kernels' tile enumeration, counting computed halves of
     diagonal tiles, rows and columns padded past the matrix and K rounded
     up to 64.  Mirrors the tile choices of the library's NS launch code:
-    128x256 single-CTA tiles or 256x256 CTA-pair tiles (SYRK/POLY on pairs
-    when 256-row pair tiles waste at most 1/8 of the rows, UPDATE at 1/16),
+    128x256 single-CTA tiles or 256x256 CTA-pair tiles (every stage on pairs
+    when 256-row pair tiles waste at most 1/8 of the rows),
     the last column tile rounded to 16 (single), 32 (pairs) or 128 (pairs on
     64-aligned shapes)."""
     pad = _ceil(mp, 256) * 256 - mp
@@ -113,7 +113,7 @@ def ns_stage_issued_flops(mp: int, np_: int):
         return total
 
     k_x, k_g = _ceil(np_, 64) * 64, _ceil(mp, 64) * 64
-    if pad * 16 <= mp:
+    if pad * 8 <= mp:
         upd = _ceil(mp, 256) * 256 * sum(col_widths(np_, True)) * k_g
     else:
         upd = _ceil(mp, 128) * 128 * sum(col_widths(np_, False)) * k_g

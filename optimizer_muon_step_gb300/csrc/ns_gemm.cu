@@ -54,10 +54,20 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
-constexpr int STAGES = 4;
+// A ring stage holds KPS consecutive 64-deep k-blocks: the MMA thread waits
+// on one barrier per stage, and fewer, larger stages cut that per-k-block
+// round trip (a wait on the full barrier and the tcgen05 fence after it).
+// Measured on CTA pairs: two k-blocks per stage took 8-9% fewer MMA-thread
+// cycles than one; three (two stages in the ring) starved the MMA.
+#ifndef MUON_KPS_SINGLE
+#define MUON_KPS_SINGLE 1
+#endif
+constexpr int KPS = MUON_KPS_SINGLE;             // single-CTA kernel: k-blocks per stage
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SUB_BYTES = A_BYTES + B_BYTES;     // one k-block
+constexpr int STAGES = 4 / KPS;
+constexpr int STAGE_BYTES = KPS * SUB_BYTES;
 #ifndef MUON_EPI_WARPS
 #define MUON_EPI_WARPS 4
 #endif
@@ -595,15 +605,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             const Tile tile = decode_tile<MODE>(p, t);
             const GroupParams& g = p.g[tile.group];
             const int nk = (g.K + BK - 1) / BK;
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb0 = 0; kb0 < nk; kb0 += KPS) {
                 if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 const uint32_t fb = smem_u32(&full_bar[stage]);
-                const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
-                const uint32_t sb = sa + A_BYTES;
-                mbar_expect_tx(fb, STAGE_BYTES);
+                const int nsub = nk - kb0 < KPS ? nk - kb0 : KPS;
+                mbar_expect_tx(fb, SUB_BYTES * nsub);
                 auto load3 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
                     tma_load_3d(dst, map, c0, c1, c2, fb);
                 };
@@ -611,26 +620,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
                     tma_load_4d(dst, map, c0, c1, c2, c3, fb);
                 };
                 const bool chunked = g.chunked != 0;
-                // A operand: 128 rows of row block ti (POLY/UPDATE read the
-                // symmetric factor transposed left of the diagonal block)
-                if (MODE != MODE_SYRK && read_transposed(kb, tile.ti, 1))
-                    load_mn(sa, &g.tm_t, chunked, 2, tile.ti * BM, BM / 64, kb, tile.mat, load3, load4);
-                else
-                    tma_load_3d(sa, &g.tm_a, kb * BK, tile.ti * BM, tile.mat, fb);
-                // B operand: 256 rows = row blocks 2tj and 2tj+1; UPDATE reads X
-                // MN-major (4 chunks per copy), POLY each half per its own block
-                const int n0 = tile.tj * BN;
-                const bool t0 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj, 1));
-                const bool t1 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj + 1, 1));
-                if (MODE == MODE_UPDATE)
-                    load_mn(sb, &g.tm_b, chunked, 4, n0, BN / 64, kb, tile.mat, load3, load4);
-                else if (t0)
-                    load_mn(sb, &g.tm_t, chunked, 2, n0, BN / 64, kb, tile.mat, load3, load4);
-                else if (t1) {
-                    tma_load_3d(sb, &g.tm_a, kb * BK, n0, tile.mat, fb);  // 128 K-major rows
-                    load_mn(sb + A_BYTES, &g.tm_t, chunked, 2, n0 + BM, BM / 64, kb, tile.mat, load3, load4);
-                } else {
-                    tma_load_3d(sb, &g.tm_b, kb * BK, n0, tile.mat, fb);
+                for (int q = 0; q < nsub; ++q) {
+                    const int kb = kb0 + q;
+                    const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES + q * SUB_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    // A operand: 128 rows of row block ti (POLY/UPDATE read the
+                    // symmetric factor transposed left of the diagonal block)
+                    if (MODE != MODE_SYRK && read_transposed(kb, tile.ti, 1))
+                        load_mn(sa, &g.tm_t, chunked, 2, tile.ti * BM, BM / 64, kb, tile.mat, load3, load4);
+                    else
+                        tma_load_3d(sa, &g.tm_a, kb * BK, tile.ti * BM, tile.mat, fb);
+                    // B operand: 256 rows = row blocks 2tj and 2tj+1; UPDATE reads X
+                    // MN-major (4 chunks per copy), POLY each half per its own block
+                    const int n0 = tile.tj * BN;
+                    const bool t0 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj, 1));
+                    const bool t1 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj + 1, 1));
+                    if (MODE == MODE_UPDATE)
+                        load_mn(sb, &g.tm_b, chunked, 4, n0, BN / 64, kb, tile.mat, load3, load4);
+                    else if (t0)
+                        load_mn(sb, &g.tm_t, chunked, 2, n0, BN / 64, kb, tile.mat, load3, load4);
+                    else if (t1) {
+                        tma_load_3d(sb, &g.tm_a, kb * BK, n0, tile.mat, fb);  // 128 K-major rows
+                        load_mn(sb + A_BYTES, &g.tm_t, chunked, 2, n0 + BM, BM / 64, kb, tile.mat, load3, load4);
+                    } else {
+                        tma_load_3d(sb, &g.tm_b, kb * BK, n0, tile.mat, fb);
+                    }
                 }
                 last_parity[stage] = static_cast<int>(phase);
                 if (++stage == STAGES) {
@@ -666,33 +680,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
             const int rem = g.N - tile.tj * BN;
             if (rem < BN) n_hi = (rem + 15) & ~15;
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb0 = 0; kb0 < nk; kb0 += KPS) {
                 if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
-                const uint32_t sb = sa + A_BYTES;
-                // the same layout choices as the producer's
-                const bool ta = MODE != MODE_SYRK && read_transposed(kb, tile.ti, 1);
-                const bool t0 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj, 1));
-                const bool t1 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj + 1, 1));
-                // one MMA over [n_lo, n_hi), or one per half when the halves'
-                // layouts differ and both are computed
-                const bool split = t0 != t1 && n_lo < BN / 2 && n_hi > BN / 2;
-                const int seg_lo[2] = {n_lo, BN / 2};
-                const int seg_hi[2] = {split ? BN / 2 : n_hi, n_hi};
-                const bool seg_t[2] = {n_lo >= BN / 2 ? t1 : t0, t1};
-#pragma unroll
-                for (int sg = 0; sg < 2; ++sg) {
-                    if (sg == 1 && !split) break;
-                    const uint32_t idesc = instr_desc(BM, seg_hi[sg] - seg_lo[sg], ta, seg_t[sg]);
-                    const uint32_t b_base = sb + static_cast<uint32_t>(seg_lo[sg]) * 128;
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        tc_mma(d_tmem + static_cast<uint32_t>(seg_lo[sg]), operand_desc(sa, k, ta),
-                               operand_desc(b_base, k, seg_t[sg]), idesc, (kb | k) != 0 ? 1u : 0u);
+                const int nsub = nk - kb0 < KPS ? nk - kb0 : KPS;
+                for (int q = 0; q < nsub; ++q) {
+                    const int kb = kb0 + q;
+                    const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES + q * SUB_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    // the same layout choices as the producer's
+                    const bool ta = MODE != MODE_SYRK && read_transposed(kb, tile.ti, 1);
+                    const bool t0 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj, 1));
+                    const bool t1 = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, 2 * tile.tj + 1, 1));
+                    // one MMA over [n_lo, n_hi), or one per half when the halves'
+                    // layouts differ and both are computed
+                    const bool split = t0 != t1 && n_lo < BN / 2 && n_hi > BN / 2;
+                    const int seg_lo[2] = {n_lo, BN / 2};
+                    const int seg_hi[2] = {split ? BN / 2 : n_hi, n_hi};
+                    const bool seg_t[2] = {n_lo >= BN / 2 ? t1 : t0, t1};
+    #pragma unroll
+                    for (int sg = 0; sg < 2; ++sg) {
+                        if (sg == 1 && !split) break;
+                        const uint32_t idesc = instr_desc(BM, seg_hi[sg] - seg_lo[sg], ta, seg_t[sg]);
+                        const uint32_t b_base = sb + static_cast<uint32_t>(seg_lo[sg]) * 128;
+    #pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            tc_mma(d_tmem + static_cast<uint32_t>(seg_lo[sg]), operand_desc(sa, k, ta),
+                                   operand_desc(b_base, k, seg_t[sg]), idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
                 }
                 tc_commit(smem_u32(&empty_bar[stage]));
                 if (++stage == STAGES) {
@@ -761,10 +779,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
 // accumulator-full barriers; both CTAs' epilogue warps arrive on the even
 // CTA's accumulator-empty barrier.  The epilogue is the single-CTA one.
 // ---------------------------------------------------------------------------
-constexpr int PSTAGES = 6;
+constexpr int PKPS = 2;                          // k-blocks per stage (see KPS)
+constexpr int PSTAGES = 6 / PKPS;
 constexpr int PA_BYTES = BM * BK * 2;            // this CTA's 128 rows of A
 constexpr int PB_BYTES = (BN / 2) * BK * 2;      // this CTA's half of B
-constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr int PSUB_BYTES = PA_BYTES + PB_BYTES;  // one k-block
+constexpr int PSTAGE_BYTES = PKPS * PSUB_BYTES;
 constexpr int PBAR_BYTES = 512;
 constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + EBUFS_BYTES + PBAR_BYTES;
 
@@ -948,17 +968,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const Tile tile = decode_pair_tile<MODE>(p, t, static_cast<int>(rank));
             const GroupParams& g = p.g[tile.group];
             const int nk = (g.K + BK - 1) / BK;
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb0 = 0; kb0 < nk; kb0 += PKPS) {
                 if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 const uint32_t fb = smem_u32(&full_bar[stage]);
                 const uint32_t fb_leader = mapa_shared(fb, 0);
-                const uint32_t sa = smem_u32(tiles + stage * PSTAGE_BYTES);
-                const uint32_t sb = sa + PA_BYTES;
                 const int b0 = tile.tj * BN + static_cast<int>(rank) * (pair_tile_n(g, tile.tj) / 2);
-                if (rank == 0) mbar_expect_tx(fb, 2 * PSTAGE_BYTES);
+                const int nsub = nk - kb0 < PKPS ? nk - kb0 : PKPS;
+                if (rank == 0) mbar_expect_tx(fb, 2 * PSUB_BYTES * nsub);
                 auto load3 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
                     tma_load_3d_pair(dst, map, c0, c1, c2, fb_leader);
                 };
@@ -966,16 +985,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     tma_load_4d_pair(dst, map, c0, c1, c2, c3, fb_leader);
                 };
                 const bool chunked = g.chunked != 0;
-                // row blocks of 256 (the pair tile): both CTAs make the same choices
-                if (MODE != MODE_SYRK && read_transposed(kb, tile.ti >> 1, 2))
-                    load_mn(sa, &g.tm_t, chunked, 2, tile.ti * BM, BM / 64, kb, tile.mat, load3, load4);
-                else
-                    tma_load_3d_pair(sa, &g.tm_a, kb * BK, tile.ti * BM, tile.mat, fb_leader);
-                if (MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, tile.tj, 2)))
-                    load_mn(sb, MODE == MODE_UPDATE ? &g.tm_b : &g.tm_t, chunked, 2, b0, BN / 2 / 64, kb, tile.mat,
-                            load3, load4);
-                else
-                    tma_load_3d_pair(sb, &g.tm_b, kb * BK, b0, tile.mat, fb_leader);
+                for (int q = 0; q < nsub; ++q) {
+                    const int kb = kb0 + q;
+                    const uint32_t sa = smem_u32(tiles + stage * PSTAGE_BYTES + q * PSUB_BYTES);
+                    const uint32_t sb = sa + PA_BYTES;
+                    // row blocks of 256 (the pair tile): both CTAs make the same choices
+                    if (MODE != MODE_SYRK && read_transposed(kb, tile.ti >> 1, 2))
+                        load_mn(sa, &g.tm_t, chunked, 2, tile.ti * BM, BM / 64, kb, tile.mat, load3, load4);
+                    else
+                        tma_load_3d_pair(sa, &g.tm_a, kb * BK, tile.ti * BM, tile.mat, fb_leader);
+                    if (MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, tile.tj, 2)))
+                        load_mn(sb, MODE == MODE_UPDATE ? &g.tm_b : &g.tm_t, chunked, 2, b0, BN / 2 / 64, kb, tile.mat,
+                                load3, load4);
+                    else
+                        tma_load_3d_pair(sb, &g.tm_b, kb * BK, b0, tile.mat, fb_leader);
+                }
                 last_parity[stage] = static_cast<int>(phase);
                 if (++stage == PSTAGES) {
                     stage = 0;
@@ -1003,21 +1027,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const int n = pair_tile_n(g, tile.tj);
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb0 = 0; kb0 < nk; kb0 += PKPS) {
                 if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(tiles + stage * PSTAGE_BYTES);
-                const uint32_t sb = sa + PA_BYTES;
-                const bool ta = MODE != MODE_SYRK && read_transposed(kb, tile.ti >> 1, 2);
-                const bool tb = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, tile.tj, 2));
-                const uint32_t idesc = instr_desc(2 * BM, n, ta, tb);
-#pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    tc_mma_pair(d_tmem, operand_desc(sa, k, ta), operand_desc(sb, k, tb), idesc,
-                                (kb | k) != 0 ? 1u : 0u);
+                const int nsub = nk - kb0 < PKPS ? nk - kb0 : PKPS;
+                for (int q = 0; q < nsub; ++q) {
+                    const int kb = kb0 + q;
+                    const uint32_t sa = smem_u32(tiles + stage * PSTAGE_BYTES + q * PSUB_BYTES);
+                    const uint32_t sb = sa + PA_BYTES;
+                    const bool ta = MODE != MODE_SYRK && read_transposed(kb, tile.ti >> 1, 2);
+                    const bool tb = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, tile.tj, 2));
+                    const uint32_t idesc = instr_desc(2 * BM, n, ta, tb);
+    #pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        tc_mma_pair(d_tmem, operand_desc(sa, k, ta), operand_desc(sb, k, tb), idesc,
+                                    (kb | k) != 0 ? 1u : 0u);
+                }
                 tc_commit_pair_mc(smem_u32(&empty_bar[stage]), 0x3);
                 if (++stage == PSTAGES) {
                     stage = 0;
@@ -1272,19 +1300,16 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first
     return cudaGetLastError();
 }
 
-// Whether a shape group runs a stage on CTA pairs.  Pairs halve each SM's
-// operand traffic and deepen the pipeline (measured 2% faster on 2048-row
-// matrices, 11% on 7168-row ones), but waste the rows of a part-empty last
-// pair row.  UPDATE pays that waste in full and takes pairs only when it is
-// at most 1/16 of the rows; SYRK and POLY, whose diagonal tiles are partly
-// redundant anyway, still gain at 1/8 (m' = 1408, 9% waste: POLY 7% faster,
-// SYRK even, UPDATE 5% slower).  SYRK and POLY always agree, so A and B are
-// stored in the same band layout; a 256-row band holds every block a
-// single-CTA UPDATE reads, so a single-CTA UPDATE may follow pair-run SYRK
-// and POLY (the reverse never occurs: 1/16 <= 1/8).
-bool use_pairs(const NsGroup& g, int mode) {
+// Whether a shape group runs on CTA pairs (all three stages).  Pairs halve
+// each SM's operand traffic and deepen the pipeline (measured 2% faster on
+// 2048-row matrices, 11% on 7168-row ones), but compute the padded rows of
+// a part-empty last pair row.  A group takes pairs when those are at most
+// 1/8 of its rows.  With two k-blocks per pair-ring stage this includes
+// the 1408-row MoE experts (9% padded rows) in every stage: their UPDATE
+// on pairs measured 1.7% faster than on single CTAs.
+bool use_pairs(const NsGroup& g) {
     const int64_t padded = (g.mp + 2 * BM - 1) / (2 * BM) * (2 * BM);
-    return (padded - g.mp) * (mode == MODE_UPDATE ? 16 : 8) <= g.mp;
+    return (padded - g.mp) * 8 <= g.mp;
 }
 
 template <int MODE>
@@ -1312,26 +1337,20 @@ cudaError_t launch_wait_probe(int* status, long long limit_ns, cudaStream_t st) 
 
 cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, const float* coeffs, int* status, int num_sms,
                    cudaStream_t st) {
-    // [0]: SYRK and POLY, [1]: UPDATE
-    std::vector<NsGroup> pairs[2], singles[2];
-    for (int i = 0; i < ngroups; ++i) {
-        (use_pairs(groups[i], MODE_SYRK) ? pairs[0] : singles[0]).push_back(groups[i]);
-        (use_pairs(groups[i], MODE_UPDATE) ? pairs[1] : singles[1]).push_back(groups[i]);
-    }
-    const int np0 = static_cast<int>(pairs[0].size()), ns0 = static_cast<int>(singles[0].size());
-    const int np1 = static_cast<int>(pairs[1].size()), ns1 = static_cast<int>(singles[1].size());
+    std::vector<NsGroup> pairs, singles;
+    for (int i = 0; i < ngroups; ++i) (use_pairs(groups[i]) ? pairs : singles).push_back(groups[i]);
+    const int np = static_cast<int>(pairs.size()), ns = static_cast<int>(singles.size());
     for (int s = 0; s < steps; ++s) {
         const int cur = s & 1;
         const float a = coeffs[3 * s], b = coeffs[3 * s + 1], c = coeffs[3 * s + 2];
         const bool first = s == 0;
-        cudaError_t e = run_stage<MODE_SYRK>(pairs[0].data(), np0, singles[0].data(), ns0, cur, first, a, b, c,
-                                             status, num_sms, st);
+        cudaError_t e =
+            run_stage<MODE_SYRK>(pairs.data(), np, singles.data(), ns, cur, first, a, b, c, status, num_sms, st);
         if (e == cudaSuccess)
-            e = run_stage<MODE_POLY>(pairs[0].data(), np0, singles[0].data(), ns0, cur, first, a, b, c, status,
-                                     num_sms, st);
+            e = run_stage<MODE_POLY>(pairs.data(), np, singles.data(), ns, cur, first, a, b, c, status, num_sms, st);
         if (e == cudaSuccess)
-            e = run_stage<MODE_UPDATE>(pairs[1].data(), np1, singles[1].data(), ns1, cur, first, a, b, c, status,
-                                       num_sms, st);
+            e = run_stage<MODE_UPDATE>(pairs.data(), np, singles.data(), ns, cur, first, a, b, c, status, num_sms,
+                                       st);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
