@@ -701,12 +701,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
                     const int seg_lo[2] = {n_lo, BN / 2};
                     const int seg_hi[2] = {split ? BN / 2 : n_hi, n_hi};
                     const bool seg_t[2] = {n_lo >= BN / 2 ? t1 : t0, t1};
-    #pragma unroll
+#pragma unroll
                     for (int sg = 0; sg < 2; ++sg) {
                         if (sg == 1 && !split) break;
                         const uint32_t idesc = instr_desc(BM, seg_hi[sg] - seg_lo[sg], ta, seg_t[sg]);
                         const uint32_t b_base = sb + static_cast<uint32_t>(seg_lo[sg]) * 128;
-    #pragma unroll
+#pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
                             tc_mma(d_tmem + static_cast<uint32_t>(seg_lo[sg]), operand_desc(sa, k, ta),
                                    operand_desc(b_base, k, seg_t[sg]), idesc, (kb | k) != 0 ? 1u : 0u);
@@ -1041,7 +1041,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     const bool ta = MODE != MODE_SYRK && read_transposed(kb, tile.ti >> 1, 2);
                     const bool tb = MODE == MODE_UPDATE || (MODE == MODE_POLY && read_transposed(kb, tile.tj, 2));
                     const uint32_t idesc = instr_desc(2 * BM, n, ta, tb);
-    #pragma unroll
+#pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         tc_mma_pair(d_tmem, operand_desc(sa, k, ta), operand_desc(sb, k, tb), idesc,
                                     (kb | k) != 0 ? 1u : 0u);
