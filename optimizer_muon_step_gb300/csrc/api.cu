@@ -321,8 +321,8 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
     int max_tiles = 1;       // flat tiles, every matrix (gradient guard)
     int max_wide_tiles = 0;  // flat tiles of the wide matrices (momentum pass)
     int max_units = 0;       // tall-pass units (momentum pass)
+    int64_t max_final_units = 0;  // tall units of the final update
     int tall_units[2] = {0, 0};  // the same, over tall matrices with fp32 / bf16 gradients
-    int64_t max_rows = 1, max_cols = 1;
 
     // Fills `descs` and the layout for plan rows [b, e) and uploads them.
     auto prepare_chunk = [&](size_t b, size_t e) -> muon_status_t {
@@ -333,8 +333,8 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
         descs.assign(n, MatDesc{});
         max_tiles = 1;
         max_wide_tiles = max_units = 0;
+        max_final_units = 0;
         tall_units[0] = tall_units[1] = 0;
-        max_rows = max_cols = 1;
         for (int k = 0; k < n; ++k) {
             const PlanRow& row = plan[b + k];
             const muon_matrix_t& m = mats[row.idx];
@@ -373,14 +373,13 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
                 d.tall_kr = static_cast<int32_t>(kr);
                 d.nparts = static_cast<int32_t>(cu * ((rt + kr - 1) / kr));
                 max_units = std::max(max_units, d.nparts);
+                max_final_units = std::max(max_final_units, final_update_tall_units(m.rows, m.cols));
                 tall_units[d.g_bf16] = std::max(tall_units[d.g_bf16], d.nparts);
             } else {
                 d.nparts = d.ntiles;
                 max_wide_tiles = std::max(max_wide_tiles, d.ntiles);
             }
             max_tiles = std::max(max_tiles, d.ntiles);
-            max_rows = std::max(max_rows, m.rows);
-            max_cols = std::max(max_cols, m.cols);
         }
         // the first NS step applies each matrix's ns_scale, read from its record
         for (size_t gi = 0; gi < L.groups.size(); ++gi) {
@@ -430,7 +429,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
         s = from_cuda(ns_run(L.groups.data(), static_cast<int>(L.groups.size()), hp->ns_steps, coeffs.data(),
                              &header->status, num_sms, st));
         if (s != MUON_OK) return s;
-        s = from_cuda(launch_final_update(d_descs, n, max_rows, max_cols, us, st));
+        s = from_cuda(launch_final_update(d_descs, n, max_wide_tiles, max_final_units, us, st));
         if (s != MUON_OK) return s;
     }
     return MUON_OK;

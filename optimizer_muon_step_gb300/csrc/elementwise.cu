@@ -374,71 +374,150 @@ __device__ __forceinline__ float update_elem(float w, float o, float sc, const U
     return __fsub_rn(w, delta);
 }
 
-__global__ void __launch_bounds__(kThreads) final_update_kernel(const MatDesc* __restrict__ descs,
-                                                                UpdateScalars us) {
-    __shared__ uint16_t tileT[kTile][kTile + 2];
-    const MatDesc& d = descs[blockIdx.z];
-    const int64_t rows = d.rows, cols = d.cols;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kTile;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTile;
-    if (r0 >= rows || c0 >= cols) return;
+// Final update of wide matrices (rows <= cols, O in the caller's layout) over
+// the momentum pass's flat tiles: one CTA per tile of tile_len elements,
+// 8 elements a thread per iteration.  grid = (max tiles, matrices).
+__global__ void __launch_bounds__(kThreads) final_update_wide_kernel(const MatDesc* __restrict__ descs,
+                                                                     UpdateScalars us) {
+    const MatDesc& d = descs[blockIdx.y];
+    const int tile = blockIdx.x;
+    if (d.transposed || tile >= d.ntiles) return;
     if (us.header && us.header->skip) return;
     const float sc = d.update_scale;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const bool full = d.vec && (cols % 4 == 0) && r0 + kTile <= rows && c0 + kTile <= cols;
     float* __restrict__ W = d.W;
     const uint16_t* __restrict__ O = d.O;
-    const int64_t ldx = d.ldx;
-    const bool tr = d.transposed != 0;
-    if (tr) {
+    const int64_t cols = d.cols, ldx = d.ldx;
+    const int64_t n = d.rows * cols;
+    const int64_t start = static_cast<int64_t>(tile) * d.tile_len;
+    const int64_t end = min(n, start + d.tile_len);
+    int64_t scalar_from = start;
+    if (d.vec && ldx == cols) {
+        const int64_t nvec = (end - start) >> 3;
+        for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
+            const int64_t i = start + (v << 3);
+            float4* wp = reinterpret_cast<float4*>(W + i);
+            float4 a = wp[0], b = wp[1];
+            const uint4 o = *reinterpret_cast<const uint4*>(O + i);
+            a.x = update_elem(a.x, __uint_as_float(o.x << 16), sc, us);
+            a.y = update_elem(a.y, __uint_as_float(o.x & 0xffff0000u), sc, us);
+            a.z = update_elem(a.z, __uint_as_float(o.y << 16), sc, us);
+            a.w = update_elem(a.w, __uint_as_float(o.y & 0xffff0000u), sc, us);
+            b.x = update_elem(b.x, __uint_as_float(o.z << 16), sc, us);
+            b.y = update_elem(b.y, __uint_as_float(o.z & 0xffff0000u), sc, us);
+            b.z = update_elem(b.z, __uint_as_float(o.w << 16), sc, us);
+            b.w = update_elem(b.w, __uint_as_float(o.w & 0xffff0000u), sc, us);
+            wp[0] = a;
+            wp[1] = b;
+        }
+        scalar_from = start + (nvec << 3);
+    }
+    for (int64_t i = scalar_from + threadIdx.x; i < end; i += kThreads)
+        W[i] = update_elem(W[i], bf16_to_f32(O[(i / cols) * ldx + i % cols]), sc, us);
+}
+
+// Final update of tall matrices (rows > cols, O holds the transpose): a CTA
+// takes one 64-column tile by up to kFinalRowTiles 64-row tiles (units in
+// column-tile order), O^T staged through shared memory.  The next tile's O
+// and W are loaded into registers right after the current tile's update, so
+// they are in flight during its barrier.  grid = (max units, matrices).
+constexpr int kFinalRowTiles = 4;
+
+inline __host__ __device__ int64_t final_tall_units(int64_t rows, int64_t cols) {
+    const int64_t rt = (rows + kTile - 1) / kTile;
+    return (cols + kTile - 1) / kTile * ((rt + kFinalRowTiles - 1) / kFinalRowTiles);
+}
+
+__global__ void __launch_bounds__(kThreads, 4) final_update_tall_kernel(const MatDesc* __restrict__ descs,
+                                                                        UpdateScalars us) {
+    __shared__ uint16_t tileT[kTile][kTile + 2];
+    const MatDesc& d = descs[blockIdx.y];
+    const int unit = blockIdx.x;
+    if (!d.transposed) return;
+    const int64_t rows = d.rows, cols = d.cols, ldx = d.ldx;
+    if (unit >= final_tall_units(rows, cols)) return;
+    if (us.header && us.header->skip) return;
+    const float sc = d.update_scale;
+    float* __restrict__ W = d.W;
+    const uint16_t* __restrict__ O = d.O;
+    // tile counts fit 32 bits: rows, cols <= 2^30
+    const int ctiles = static_cast<int>((cols + kTile - 1) / kTile);
+    const int64_t c0u = static_cast<int64_t>(unit % ctiles) * kTile;
+    const int rt_begin = (unit / ctiles) * kFinalRowTiles;
+    const int rt_end = min(static_cast<int>((rows + kTile - 1) / kTile), rt_begin + kFinalRowTiles);
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int ntl = rt_end - rt_begin;
+    auto origin = [&](int t, int64_t& r0, int64_t& c0) {
+        c0 = c0u;
+        r0 = static_cast<int64_t>(rt_begin + t) * kTile;
+    };
+    auto is_full = [&](int64_t r0, int64_t c0) {
+        return d.vec && (cols % 4 == 0) && r0 + kTile <= rows && c0 + kTile <= cols;
+    };
+    // registers of one full tile: O rows c0 + ty + 16 i, columns r0 + 4 tx ..;
+    // W rows r0 + ty + 16 i, columns c0 + 4 tx ..
+    uint2 oreg[4];
+    float4 wreg[4];
+    auto load_full = [&](int64_t r0, int64_t c0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            oreg[i] = *reinterpret_cast<const uint2*>(O + (c0 + ty + 16 * i) * ldx + r0 + 4 * tx);
+            wreg[i] = *reinterpret_cast<const float4*>(W + (r0 + ty + 16 * i) * cols + c0 + 4 * tx);
+        }
+    };
+    bool loaded = false;  // the registers hold tile t
+    for (int t = 0; t < ntl; ++t) {
+        int64_t r0, c0;
+        origin(t, r0, c0);
+        const bool full = is_full(r0, c0);
+        if (full && !loaded) load_full(r0, c0);
         // stage O^T: O rows c0.., columns r0..
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int cl = ty + 16 * i;
-            const int64_t orow = c0 + cl;
-            const int64_t ocol = r0 + 4 * tx;
             if (full) {
-                uint2 raw = *reinterpret_cast<const uint2*>(O + orow * ldx + ocol);
-                tileT[cl][4 * tx] = raw.x & 0xffffu; tileT[cl][4 * tx + 1] = raw.x >> 16;
-                tileT[cl][4 * tx + 2] = raw.y & 0xffffu; tileT[cl][4 * tx + 3] = raw.y >> 16;
+                tileT[cl][4 * tx] = oreg[i].x & 0xffffu;
+                tileT[cl][4 * tx + 1] = oreg[i].x >> 16;
+                tileT[cl][4 * tx + 2] = oreg[i].y & 0xffffu;
+                tileT[cl][4 * tx + 3] = oreg[i].y >> 16;
             } else {
+                const int64_t orow = c0 + cl;
+                const int64_t ocol = r0 + 4 * tx;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     tileT[cl][4 * tx + j] = (orow < cols && ocol + j < rows) ? O[orow * ldx + ocol + j] : 0;
             }
         }
         __syncthreads();
-    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int rl = ty + 16 * i;
-        const int64_t r = r0 + rl;
-        const int64_t c = c0 + 4 * tx;
-        if (full) {
-            float4* wp = reinterpret_cast<float4*>(W + r * cols + c);
-            float4 w4 = *wp;
-            uint16_t o[4];
-            if (tr) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) o[j] = tileT[4 * tx + j][rl];
+        for (int i = 0; i < 4; ++i) {
+            const int rl = ty + 16 * i;
+            const int64_t r = r0 + rl;
+            const int64_t c = c0 + 4 * tx;
+            if (full) {
+                float4 w4 = wreg[i];
+                w4.x = update_elem(w4.x, bf16_to_f32(tileT[4 * tx][rl]), sc, us);
+                w4.y = update_elem(w4.y, bf16_to_f32(tileT[4 * tx + 1][rl]), sc, us);
+                w4.z = update_elem(w4.z, bf16_to_f32(tileT[4 * tx + 2][rl]), sc, us);
+                w4.w = update_elem(w4.w, bf16_to_f32(tileT[4 * tx + 3][rl]), sc, us);
+                *reinterpret_cast<float4*>(W + r * cols + c) = w4;
             } else {
-                uint2 raw = *reinterpret_cast<const uint2*>(O + r * ldx + c);
-                o[0] = raw.x & 0xffffu; o[1] = raw.x >> 16; o[2] = raw.y & 0xffffu; o[3] = raw.y >> 16;
-            }
-            w4.x = update_elem(w4.x, bf16_to_f32(o[0]), sc, us);
-            w4.y = update_elem(w4.y, bf16_to_f32(o[1]), sc, us);
-            w4.z = update_elem(w4.z, bf16_to_f32(o[2]), sc, us);
-            w4.w = update_elem(w4.w, bf16_to_f32(o[3]), sc, us);
-            *wp = w4;
-        } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (r < rows && c + j < cols) {
-                    uint16_t o = tr ? tileT[4 * tx + j][rl] : O[r * ldx + c + j];
-                    W[r * cols + c + j] = update_elem(W[r * cols + c + j], bf16_to_f32(o), sc, us);
-                }
+                for (int j = 0; j < 4; ++j)
+                    if (r < rows && c + j < cols)
+                        W[r * cols + c + j] = update_elem(W[r * cols + c + j], bf16_to_f32(tileT[4 * tx + j][rl]), sc, us);
             }
         }
+        // the next tile's loads go out before this tile's closing barrier
+        loaded = false;
+        if (t + 1 < ntl) {
+            int64_t r1, c1;
+            origin(t + 1, r1, c1);
+            if (is_full(r1, c1)) {
+                load_full(r1, c1);
+                loaded = true;
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -626,6 +705,8 @@ cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles,
     return cudaGetLastError();
 }
 
+int64_t final_update_tall_units(int64_t rows, int64_t cols) { return final_tall_units(rows, cols); }
+
 cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, int force_rescale, cudaStream_t st) {
     const int per = kThreads / 32;
     launch_begin(MUON_KERNEL_NORM_FINALIZE, st);
@@ -637,16 +718,22 @@ cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, int force
     return cudaGetLastError();
 }
 
-cudaError_t launch_final_update(const MatDesc* descs, int count, int64_t max_rows, int64_t max_cols,
+cudaError_t launch_final_update(const MatDesc* descs, int count, int max_wide_tiles, int64_t max_tall_units,
                                 UpdateScalars s, cudaStream_t st) {
-    const unsigned gx = static_cast<unsigned>((max_cols + kTile - 1) / kTile);
-    const unsigned gy = static_cast<unsigned>((max_rows + kTile - 1) / kTile);
-    if (gy > 65535u) return cudaErrorInvalidValue;
+    if (max_tall_units > 0x7fffffff) return cudaErrorInvalidValue;
     for (int off = 0; off < count; off += 65535) {
         int n = count - off < 65535 ? count - off : 65535;
-        launch_begin(MUON_KERNEL_FINAL_UPDATE, st);
-        final_update_kernel<<<dim3(gx, gy, n), kThreads, 0, st>>>(descs + off, s);
-        launch_end(MUON_KERNEL_FINAL_UPDATE, st);
+        if (max_wide_tiles > 0) {
+            launch_begin(MUON_KERNEL_FINAL_UPDATE, st);
+            final_update_wide_kernel<<<dim3(max_wide_tiles, n), kThreads, 0, st>>>(descs + off, s);
+            launch_end(MUON_KERNEL_FINAL_UPDATE, st);
+        }
+        if (max_tall_units > 0) {
+            launch_begin(MUON_KERNEL_FINAL_UPDATE, st);
+            final_update_tall_kernel<<<dim3(static_cast<unsigned>(max_tall_units), n), kThreads, 0, st>>>(descs + off,
+                                                                                                       s);
+            launch_end(MUON_KERNEL_FINAL_UPDATE, st);
+        }
     }
     return cudaGetLastError();
 }

@@ -92,8 +92,13 @@ cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles,
 // 2^-k: exact, the NS result is unchanged).  With `force_rescale` (no NS
 // step follows) X0 = bf16(X0 * scale) and ns_scale = 1.
 cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, int force_rescale, cudaStream_t st);
-cudaError_t launch_final_update(const MatDesc* descs, int count, int64_t max_rows,
-                                int64_t max_cols, UpdateScalars s, cudaStream_t st);
+// Final update: wide matrices over the momentum pass's flat tiles
+// (max_wide_tiles bounds ntiles), tall ones over units of one 64-column tile
+// by up to four 64-row tiles (max_tall_units bounds
+// final_update_tall_units over the tall matrices).
+int64_t final_update_tall_units(int64_t rows, int64_t cols);
+cudaError_t launch_final_update(const MatDesc* descs, int count, int max_wide_tiles, int64_t max_tall_units,
+                                UpdateScalars s, cudaStream_t st);
 cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n,
                          AdamwScalars s, int num_sms, cudaStream_t st);
 // Gradient guard: per-tile sums of G^2 into the partials and a count of
