@@ -293,3 +293,20 @@ def test_step_two_steps_resume_exact(lib):
     m.muon_step_batched(Wc, G, Mc, hp)
     for a, b in zip(W + M, Wc + Mc):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("gdt", [torch.bfloat16, torch.float32])
+def test_step_ragged_tall_multi_tile_units(lib, gdt):
+    """A tall matrix with more 64x64 tiles than one momentum partial per tile
+    allows (2100 x 2050: 33 x 33 tiles), so the momentum pass walks units of
+    two row tiles (for bf16 gradients prefetching the next tile across
+    partial ones), and the final update walks units of up to four row tiles
+    with a partial last row group and a partial last column.  The momentum
+    is bit-exact; the update matches the oracle's full step."""
+    shapes = [(2100, 2050)]
+    W, G, M = make_mats(shapes, [gdt], seed=12)
+    host = [(w.cpu().numpy(), g.float().cpu().numpy(), mm.cpu().numpy()) for w, g, mm in zip(W, G, M)]
+    hp = m.MuonHparams()
+    ws = m.muon_step_batched(W, G, M, hp)
+    assert m.muon_query_status(ws) == 0
+    check_step(*host[0], W[0].cpu().numpy(), M[0].cpu().numpy(), hp)
