@@ -584,31 +584,31 @@ __global__ void __launch_bounds__(kThreads) grad_stats_kernel(const MatDesc* __r
     if (bad) atomicAdd(&header->nonfinite, static_cast<unsigned long long>(bad));
 }
 
-// One warp per matrix sums its partials in fp64 (fixed order); one thread
-// then adds the matrix sums to header->sumsq in matrix order, so the total
-// does not depend on scheduling.
-__global__ void __launch_bounds__(kThreads) grad_stats_reduce_kernel(const MatDesc* __restrict__ descs, int count,
-                                                                     WsHeader* __restrict__ header) {
-    constexpr int kBatch = 512;
-    __shared__ double msum[kBatch];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    double total = 0.0;
-    for (int base = 0; base < count; base += kBatch) {
-        const int nb = min(kBatch, count - base);
-        for (int j = warp; j < nb; j += kThreads / 32) {
-            const MatDesc& d = descs[base + j];
-            double s = 0.0;
-            for (int i = lane; i < d.ntiles; i += 32) s += static_cast<double>(d.partials[i]);
+// One warp per matrix sums its partials in fp64 in a fixed order (lane
+// strides, then a fixed shuffle tree) into the matrix's record.
+__global__ void __launch_bounds__(kThreads) grad_stats_reduce_kernel(MatDesc* __restrict__ descs, int count) {
+    const int k = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (k >= count) return;
+    MatDesc& d = descs[k];
+    double s = 0.0;
+    for (int i = lane; i < d.ntiles; i += 32) s += static_cast<double>(d.partials[i]);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) msum[j] = s;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0)
-            for (int j = 0; j < nb; ++j) total += msum[j];
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) header->sumsq += total;
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) d.gsum = s;
+}
+
+// One warp adds the matrices' sums to header->sumsq: lane l sums matrices
+// l, l + 32, ... in order, then a fixed shuffle tree, so the total does not
+// depend on scheduling.
+__global__ void __launch_bounds__(32) grad_stats_total_kernel(const MatDesc* __restrict__ descs, int count,
+                                                             WsHeader* __restrict__ header) {
+    const int lane = threadIdx.x;
+    double s = 0.0;
+    for (int k = lane; k < count; k += 32) s += descs[k].gsum;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) header->sumsq += s;
 }
 
 __global__ void grad_decide_kernel(WsHeader* __restrict__ header, float max_grad_norm, int32_t skip_nonfinite) {
@@ -750,9 +750,13 @@ cudaError_t launch_grad_stats(const MatDesc* descs, int count, int max_tiles, Ws
     return cudaGetLastError();
 }
 
-cudaError_t launch_grad_stats_reduce(const MatDesc* descs, int count, WsHeader* header, cudaStream_t st) {
+cudaError_t launch_grad_stats_reduce(MatDesc* descs, int count, WsHeader* header, cudaStream_t st) {
+    const int per = kThreads / 32;
     launch_begin(MUON_KERNEL_GRAD_GUARD, st);
-    grad_stats_reduce_kernel<<<1, kThreads, 0, st>>>(descs, count, header);
+    grad_stats_reduce_kernel<<<(count + per - 1) / per, kThreads, 0, st>>>(descs, count);
+    launch_end(MUON_KERNEL_GRAD_GUARD, st);
+    launch_begin(MUON_KERNEL_GRAD_GUARD, st);
+    grad_stats_total_kernel<<<1, 32, 0, st>>>(descs, count, header);
     launch_end(MUON_KERNEL_GRAD_GUARD, st);
     return cudaGetLastError();
 }

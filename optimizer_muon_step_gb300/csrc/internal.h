@@ -34,7 +34,7 @@ struct MatDesc {
     int32_t rescaled;    // 1: X0 is multiplied in place by rescale_factor before NS
     float rescale_factor;
     float ns_scale;      // factor the first NS step applies to X0
-    int32_t pad_[2];
+    double gsum;         // gradient guard: sum of G^2 over the matrix (fp64)
 };
 
 constexpr int kMaxNormTiles = 1024;
@@ -106,7 +106,7 @@ cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n
 // in order into header->sumsq; finally the clip factor and skip flag.
 cudaError_t launch_grad_stats(const MatDesc* descs, int count, int max_tiles, WsHeader* header,
                               cudaStream_t st);
-cudaError_t launch_grad_stats_reduce(const MatDesc* descs, int count, WsHeader* header, cudaStream_t st);
+cudaError_t launch_grad_stats_reduce(MatDesc* descs, int count, WsHeader* header, cudaStream_t st);
 cudaError_t launch_grad_decide(WsHeader* header, float max_grad_norm, int32_t skip_nonfinite,
                                cudaStream_t st);
 
