@@ -98,8 +98,10 @@ def test_workload_fp32_grads(lib, name):
 
 def test_workload_c2_dense_decoder(lib):
     w = workloads.get("c2")
-    # layer 0's q (2048x2048), gate (5632x2048, tall) and down (2048x5632)
-    sample = [0, 4, 6]
+    # the first and the last layer's q (2048x2048), gate (5632x2048, tall) and
+    # down (2048x5632); seven matrices per layer
+    last = 7 * (len(w.matrices) // 7 - 1)
+    sample = [0, 4, 6, last, last + 4, last + 6]
     # momentum of every matrix is checked element-wise against the oracle
     t0 = workloads.make_muon(w, device=DEV)
     G_all = [g.float().cpu().numpy() for g in t0.G]
