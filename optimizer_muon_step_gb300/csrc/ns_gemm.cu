@@ -772,7 +772,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
 // ---------------------------------------------------------------------------
 // CTA-pair variant: tcgen05.mma.cta_group::2 on 256x256 pair tiles.  Each
 // CTA of a 2-CTA cluster stages its own 128 rows of A and its own half (128
-// rows) of B, 32 KB per stage, six stages; the even CTA issues the MMAs,
+// rows) of B, 32 KB per 64-deep k-block, in three stages of two k-blocks
+// each; the even CTA issues the MMAs,
 // which read both CTAs' shared memory and write each CTA's 128 accumulator
 // rows into that CTA's TMEM.  Both CTAs' operand loads complete on the even
 // CTA's full barrier; its MMA commits arrive on both CTAs' empty and
