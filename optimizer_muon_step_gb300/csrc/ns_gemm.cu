@@ -1198,27 +1198,44 @@ int triangle_pair_tiles(int tiles_n) { return tiles_n * (tiles_n + 1) / 2; }
 template <int MODE, bool kPair>
 cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first, float a, float b, float c,
                          int* status, int num_sms, cudaStream_t st) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int max_pairs = 0;
-    std::call_once(attr_once, [] {
-        if (kPair) {
-            attr_err = cudaFuncSetAttribute(ns_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            PSMEM_BYTES);
-            if (attr_err == cudaSuccess) {
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3(2, 1, 1);
-                cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-                cfg.dynamicSmemBytes = PSMEM_BYTES;
-                int n = 0;
-                attr_err = cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel<MODE>, &cfg);
-                max_pairs = n;
+    // Kernel attributes and the pair occupancy, set up once per device (with
+    // that device current) and remembered.
+    constexpr int kMaxDevices = 64;
+    static std::mutex setup_mu;
+    static bool setup_done[kMaxDevices] = {};
+    static cudaError_t setup_err[kMaxDevices] = {};
+    static int setup_pairs[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t attr_err = cudaGetDevice(&dev);
+    if (attr_err != cudaSuccess) return attr_err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int max_pairs = 0;
+    {
+        std::lock_guard<std::mutex> lock(setup_mu);
+        if (!setup_done[dev]) {
+            cudaError_t e;
+            int n = 0;
+            if (kPair) {
+                e = cudaFuncSetAttribute(ns_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PSMEM_BYTES);
+                if (e == cudaSuccess) {
+                    cudaLaunchConfig_t cfg = {};
+                    cfg.gridDim = dim3(2, 1, 1);
+                    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+                    cfg.dynamicSmemBytes = PSMEM_BYTES;
+                    e = cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel<MODE>, &cfg);
+                }
+            } else {
+                e = cudaFuncSetAttribute(ns_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
             }
-        } else {
-            attr_err = cudaFuncSetAttribute(ns_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            SMEM_BYTES);
+            setup_err[dev] = e;
+            setup_pairs[dev] = n;
+            setup_done[dev] = true;
         }
-    });
+        attr_err = setup_err[dev];
+        max_pairs = setup_pairs[dev];
+    }
     if (attr_err != cudaSuccess) return attr_err;
 
     NsParams prm;
