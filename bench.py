@@ -43,7 +43,7 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 << 20  # GB300 L2
 ADAMW_BYTES_PER_PARAM = 28  # read p, g, m, v (16 B), write p, m, v (12 B)
 KINDS = ("momentum_norm", "norm_finalize", "x0_rescale", "ns_syrk", "ns_poly", "ns_update",
-         "final_update", "adamw", "grad_guard")
+         "final_update", "adamw", "grad_guard", "desc_upload")
 
 
 def parse():
@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--no-adamw", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-guard", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--subset", type=int, default=0,
                     help="profiling only: keep the first N matrices of the workload")
     ap.add_argument("--adamw-params", type=int, default=0,
@@ -573,6 +574,35 @@ def run_ours(args, rank, world, local_rank):
                  "guard_gbs": g_bytes / (guard_ms / 1e3) / 1e9, "guard_bytes_per_step": g_bytes,
                  "settings": "skip_nonfinite=1, max_grad_norm=1e9"}
 
+    # ---- the same step replayed from a captured CUDA graph ----
+    graph = None
+    if not args.no_graph:
+        g = batch.capture(hp)
+        for _ in range(2):
+            g.launch(stream)
+        torch.cuda.synchronize()
+        n_graph = max(3, min(args.steps, 20))
+        g_events = []
+        gl0 = m.muon_launch_count()
+        for _ in range(n_graph):
+            if flush is not None:
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.launch(stream)
+            b.record(stream)
+            g_events.append((a, b))
+        torch.cuda.synchronize()
+        g.destroy()
+        if m.muon_query_status(batch.workspace) != 0:
+            raise RuntimeError("device status set in the graph replays")
+        g_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in g_events)) / n_graph
+        graph = {"ms_per_step": g_ms, "value": aggregate_tflops(step_flops, n_graph, world, g_ms * n_graph),
+                 "steps": n_graph, "launches_per_step": (m.muon_launch_count() - gl0) / n_graph,
+                 "timed": "per replay, CUDA events around each graph launch"
+                          + ("; L2 flushed before each" if flush is not None else "")}
+
     # ---- end to end through the public API, host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -628,7 +658,8 @@ def run_ours(args, rank, world, local_rank):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": workload_config(w, steps_ns, world),
                 "roofline": roofline, "ns": ns_summary, "stages": stages, "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": launches, "clocks": clk, "adamw": adamw, "guarded_step": guard}
+                "e2e": e2e, "gpu_launches": launches, "clocks": clk, "adamw": adamw, "guarded_step": guard,
+                "graph_replay": graph}
         print(json.dumps(line), flush=True)
 
 

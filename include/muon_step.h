@@ -147,7 +147,10 @@ muon_status_t muon_plan(const muon_matrix_t* mats, int64_t count,
  * matrix's muon_workspace_bytes_per_matrix), 256-byte aligned; it must not
  * be used by other work until the step has finished on `stream`.
  * count == 0 is a no-op.  A kernel that gives up on a bounded wait records
- * MUON_ERR_TIMEOUT in the workspace; read it with muon_query_status. */
+ * MUON_ERR_TIMEOUT in the workspace; read it with muon_query_status.
+ * The call enqueues kernels and one memset only (no host<->device copy, no
+ * synchronisation), so it may run inside a CUDA stream capture; see
+ * muon_step_graph_create. */
 muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count,
                                 const muon_hparams_t* hp, void* workspace,
                                 size_t ws_bytes, void* stream);
@@ -180,6 +183,41 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count,
  *     caller cannot address: muon_query_status does not apply. */
 muon_status_t muon_step_batched_noalloc(const muon_matrix_t* mats, int64_t count,
                                         const muon_hparams_t* hp, void* stream);
+
+/* ---- The step as a CUDA graph (no counterpart on the pages) ------------- */
+
+/* muon_step_batched enqueues only kernels and one memset (the per-matrix
+ * records travel as kernel parameters), so a caller may capture it into a
+ * CUDA graph of its own.  The calls below do that for the caller.
+ *
+ * A captured step replays the whole launch sequence of one
+ * muon_step_batched call with everything the call read fixed at capture:
+ * the W, G, M and workspace addresses, the shapes, the plan and the
+ * hyper-parameters (lr, weight decay, momentum, NS coefficients, guard
+ * settings).  Each replay reads the current contents of G and updates W and
+ * M in place, like the eager call; to change a hyper-parameter, capture
+ * again.  Replays on one workspace must not overlap on the GPU. */
+typedef struct muon_graph_s* muon_graph_t;
+
+/* Captures one muon_step_batched call with these arguments (same meaning,
+ * same checks and errors) into a graph and instantiates it; *out receives
+ * the handle, NULL on failure.  Nothing runs on the GPU.  Must be called
+ * with the device that holds the buffers current.  Host memory the call
+ * reads (mats, hp, hp->ns_coeffs) may be freed when it returns; the device
+ * buffers must outlive the handle.  count == 0 gives a handle whose launch
+ * is a no-op. */
+muon_status_t muon_step_graph_create(const muon_matrix_t* mats, int64_t count,
+                                     const muon_hparams_t* hp, void* workspace,
+                                     size_t ws_bytes, muon_graph_t* out);
+
+/* Enqueues one replay of the captured step on `stream` (a stream of the
+ * device the graph was created on).  MUON_ERR_INVALID_ARG on a NULL
+ * handle, MUON_ERR_CUDA if the launch fails. */
+muon_status_t muon_step_graph_launch(muon_graph_t graph, void* stream);
+
+/* Frees the graph (host and driver objects; no device buffer of the
+ * caller's).  Replays already enqueued still run.  NULL is a no-op. */
+muon_status_t muon_step_graph_destroy(muon_graph_t graph);
 
 /* Newton-Schulz alone on a batch of `count` wide bf16 matrices (device,
  * [count][mp][np] row-major, bf16 bit patterns, mp <= np), writing the
@@ -237,15 +275,20 @@ typedef enum {
     MUON_KERNEL_FINAL_UPDATE = 6,   /* W -= lr (wd W + scale O)             */
     MUON_KERNEL_ADAMW = 7,          /* AdamW                                */
     MUON_KERNEL_GRAD_GUARD = 8,     /* global gradient norm / non-finite    */
-    MUON_KERNEL_COUNT = 9
+    MUON_KERNEL_DESC_UPLOAD = 9,    /* per-matrix records into the workspace */
+    MUON_KERNEL_COUNT = 10
 } muon_kernel_kind_t;
 
-/* Process-wide count of kernels this library has launched (all kinds). */
+/* Process-wide count of kernels this library has launched (all kinds); a
+ * graph replay adds the number of kernels its capture enqueued.  Launches
+ * made while a graph is captured are not counted. */
 int64_t muon_launch_count(void);
 
 /* enable != 0: from now on every launch is bracketed by two CUDA events
  * recorded on its stream (library-owned events; the launches themselves are
- * unchanged).  Enabling or disabling drops the records collected so far. */
+ * unchanged); launches inside muon_step_graph_create's capture and graph
+ * replays are not timed.  Enabling or disabling drops the records collected
+ * so far. */
 muon_status_t muon_set_timing(int32_t enable);
 
 /* Waits for the recorded events, writes the summed milliseconds and the

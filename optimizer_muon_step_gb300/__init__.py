@@ -14,6 +14,7 @@ Functions keep the C names:
     muon_workspace_bytes_per_matrix(rows, cols)
     muon_workspace_size(shapes, budget_bytes)
     muon_query_status(workspace, stream=None)
+    muon_step_graph_create / _launch / _destroy (through MuonBatch.capture)
 """
 from __future__ import annotations
 
@@ -41,9 +42,10 @@ EXPORTS = ("muon_workspace_bytes_per_matrix", "muon_workspace_size", "muon_plan"
            "muon_step_batched", "muon_newton_schulz", "adamw_step", "muon_query_status",
            "muon_status_string", "muon_version", "muon_launch_count", "muon_set_timing",
            "muon_timing_read", "muon_kernel_name", "muon_step_batched_noalloc",
-           "muon_check_bounded_wait")
+           "muon_check_bounded_wait", "muon_step_graph_create", "muon_step_graph_launch",
+           "muon_step_graph_destroy")
 KERNEL_KINDS = ("momentum_norm", "norm_finalize", "x0_rescale", "ns_syrk", "ns_poly",
-                "ns_update", "final_update", "adamw", "grad_guard")
+                "ns_update", "final_update", "adamw", "grad_guard", "desc_upload")
 
 
 class MuonError(RuntimeError):
@@ -178,6 +180,12 @@ def load_library(path: str = LIB_PATH):
         lib.muon_timing_read.restype = ctypes.c_int
         lib.muon_kernel_name.argtypes = [i32]
         lib.muon_kernel_name.restype = ctypes.c_char_p
+        lib.muon_step_graph_create.argtypes = [P, i64, P, P, ctypes.c_size_t, ctypes.POINTER(P)]
+        lib.muon_step_graph_create.restype = ctypes.c_int
+        lib.muon_step_graph_launch.argtypes = [P, P]
+        lib.muon_step_graph_launch.restype = ctypes.c_int
+        lib.muon_step_graph_destroy.argtypes = [P]
+        lib.muon_step_graph_destroy.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -426,3 +434,43 @@ class MuonBatch:
                                                 ctypes.c_void_p(self.workspace.data_ptr()),
                                                 self.workspace.numel(), _stream(stream)),
                "muon_step_batched")
+
+    def capture(self, hp: MuonHparams = MuonHparams()) -> "MuonGraph":
+        """The step with these hyper-parameters captured once as a CUDA
+        graph (muon_step_graph_create); replay it with ``MuonGraph.launch``."""
+        return MuonGraph(self, hp)
+
+
+class MuonGraph:
+    """A captured Muon step over a MuonBatch's matrices and workspace.
+
+    Every replay runs the same kernels as ``MuonBatch.step(hp)`` with the
+    hyper-parameters fixed at capture, reading the current gradients."""
+
+    def __init__(self, batch: MuonBatch, hp: MuonHparams):
+        self._batch = batch  # keeps the tensors and the workspace alive
+        self._lib = load_library()
+        h = hp._c()
+        handle = ctypes.c_void_p()
+        _check(self._lib.muon_step_graph_create(ctypes.cast(batch.arr, ctypes.c_void_p), batch.count,
+                                                ctypes.byref(h),
+                                                ctypes.c_void_p(batch.workspace.data_ptr()),
+                                                batch.workspace.numel(), ctypes.byref(handle)),
+               "muon_step_graph_create")
+        self._handle = handle
+
+    def launch(self, stream=None):
+        if self._handle is None:
+            raise RuntimeError("the graph has been destroyed")
+        _check(self._lib.muon_step_graph_launch(self._handle, _stream(stream)), "muon_step_graph_launch")
+
+    def destroy(self):
+        if getattr(self, "_handle", None) is not None:
+            _check(self._lib.muon_step_graph_destroy(self._handle), "muon_step_graph_destroy")
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass

@@ -13,7 +13,9 @@
 #include <math.h>
 
 #include <algorithm>
+#include <memory>
 #include <mutex>
+#include <new>
 #include <numeric>
 #include <vector>
 
@@ -324,7 +326,9 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
     int64_t max_final_units = 0;  // tall units of the final update
     int tall_units[2] = {0, 0};  // the same, over tall matrices with fp32 / bf16 gradients
 
-    // Fills `descs` and the layout for plan rows [b, e) and uploads them.
+    // Fills `descs` and the layout for plan rows [b, e) and uploads them (by
+    // kernel parameters: no host buffer outlives the call, so the sequence
+    // can be captured into a graph).
     auto prepare_chunk = [&](size_t b, size_t e) -> muon_status_t {
         const int n = static_cast<int>(e - b);
         layout_groups(plan, b, e, ws, L);
@@ -387,7 +391,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
                                                                 offsetof(MatDesc, ns_scale));
             L.groups[gi].scale_stride = static_cast<int64_t>(sizeof(MatDesc) / sizeof(float));
         }
-        return from_cuda(cudaMemcpyAsync(d_descs, descs.data(), sizeof(MatDesc) * n, cudaMemcpyHostToDevice, st));
+        return from_cuda(launch_desc_upload(d_descs, descs.data(), n, st));
     };
 
     // chunk boundaries
@@ -433,6 +437,76 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
         if (s != MUON_OK) return s;
     }
     return MUON_OK;
+}
+
+}  // extern "C"
+
+// A captured step: the instantiated graph and what one replay launches.
+struct muon_graph_s {
+    cudaGraphExec_t exec;  // null for a step of no matrices
+    int64_t launches;      // this library's kernels in one replay
+};
+
+extern "C" {
+
+muon_status_t muon_step_graph_create(const muon_matrix_t* mats, int64_t count, const muon_hparams_t* hp,
+                                     void* workspace, size_t ws_bytes, muon_graph_t* out) {
+    if (!out) return MUON_ERR_INVALID_ARG;
+    *out = nullptr;
+    // the host-side checks of the step, so that a bad call captures nothing
+    muon_status_t s = check_hparams(hp);
+    if (s != MUON_OK) return s;
+    s = check_shapes(mats, count);
+    if (s != MUON_OK) return s;
+    std::unique_ptr<muon_graph_s> g(new (std::nothrow) muon_graph_s{nullptr, 0});
+    if (!g) return MUON_ERR_INVALID_ARG;
+    if (count > 0) {
+        s = check_pointers(mats, count);
+        if (s != MUON_OK) return s;
+        if (!workspace) return MUON_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_ERR_MISALIGNED;
+        int num_sms = 0;
+        s = device_info(&num_sms);
+        if (s != MUON_OK) return s;
+        // kernel attributes are set outside the capture
+        if (ns_prepare_device() != cudaSuccess) return MUON_ERR_CUDA;
+        cudaStream_t cs = nullptr;
+        if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return MUON_ERR_CUDA;
+        cudaGraph_t graph = nullptr;
+        s = from_cuda(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal));
+        if (s == MUON_OK) {
+            capture_begin();
+            s = muon_step_batched(mats, count, hp, workspace, ws_bytes, cs);
+            g->launches = capture_end();
+            const cudaError_t e = cudaStreamEndCapture(cs, &graph);
+            if (s == MUON_OK && e != cudaSuccess) s = MUON_ERR_CUDA;
+        }
+        if (s == MUON_OK && cudaGraphInstantiate(&g->exec, graph, 0) != cudaSuccess) {
+            g->exec = nullptr;
+            s = MUON_ERR_CUDA;
+        }
+        if (graph) cudaGraphDestroy(graph);
+        cudaStreamDestroy(cs);
+        if (s != MUON_OK) return s;
+    }
+    *out = g.release();
+    return MUON_OK;
+}
+
+muon_status_t muon_step_graph_launch(muon_graph_t graph, void* stream) {
+    if (!graph) return MUON_ERR_INVALID_ARG;
+    if (!graph->exec) return MUON_OK;
+    if (cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) != cudaSuccess) return MUON_ERR_CUDA;
+    count_replay(graph->launches);
+    return MUON_OK;
+}
+
+muon_status_t muon_step_graph_destroy(muon_graph_t graph) {
+    if (!graph) return MUON_OK;
+    // an executable graph still in flight is freed when it completes
+    const bool ok = !graph->exec || cudaGraphExecDestroy(graph->exec) == cudaSuccess;
+    delete graph;
+    return ok ? MUON_OK : MUON_ERR_CUDA;
 }
 
 muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t count, int64_t mp, int64_t np,

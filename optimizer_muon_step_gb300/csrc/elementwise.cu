@@ -12,6 +12,8 @@
 //   grad guard      global sum of G^2 and non-finite count; clip factor
 //                   and skip decision
 //   adamw           AdamW on flat buffers
+//   desc_upload     the per-matrix records into the workspace, carried as
+//                   kernel parameters
 //
 // Formulas follow "LLM training series, part 2: optimizers" (mhpq.cn):
 // momentum as an exponential moving average (section 2.1), Adam with bias
@@ -20,6 +22,10 @@
 // __fadd_rn, ...) so no multiply-add is contracted and the results are
 // reproducible bit for bit.
 #include <cuda_bf16.h>
+#include <string.h>
+
+#include <memory>
+#include <new>
 
 #include "internal.h"
 
@@ -677,7 +683,55 @@ inline unsigned grid_for(int64_t work, int64_t per_block, int64_t cap) {
     return static_cast<unsigned>(b);
 }
 
+// Per-matrix records passed by value: one launch carries up to K of them in
+// its parameter block (kernel parameters may take up to 32764 bytes on
+// sm_70 and later), so the upload reads no host buffer after the launch and
+// a captured graph keeps the records in its kernel node.
+template <int K>
+struct DescBatch {
+    MatDesc* dst;
+    int32_t count;
+    MatDesc d[K];
+};
+constexpr int kUploadSmall = 8;
+constexpr int kUploadLarge = 224;
+static_assert(sizeof(DescBatch<kUploadLarge>) <= 32764, "kernel parameter limit");
+static_assert(sizeof(MatDesc) % 4 == 0, "word copy");
+
+template <int K>
+__global__ void __launch_bounds__(kThreads) desc_upload_kernel(const __grid_constant__ DescBatch<K> b) {
+    constexpr int kWords = static_cast<int>(sizeof(MatDesc) / 4);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(b.d);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(b.dst);
+    for (int i = threadIdx.x; i < b.count * kWords; i += blockDim.x) dst[i] = src[i];
+}
+
+template <int K>
+cudaError_t upload_batch(MatDesc* d_descs, const MatDesc* descs, int count, cudaStream_t st) {
+    std::unique_ptr<DescBatch<K>> b(new (std::nothrow) DescBatch<K>());
+    if (!b) return cudaErrorMemoryAllocation;
+    b->dst = d_descs;
+    b->count = count;
+    memcpy(b->d, descs, sizeof(MatDesc) * static_cast<size_t>(count));
+    launch_begin(MUON_KERNEL_DESC_UPLOAD, st);
+    desc_upload_kernel<K><<<1, kThreads, 0, st>>>(*b);
+    launch_end(MUON_KERNEL_DESC_UPLOAD, st);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_desc_upload(MatDesc* d_descs, const MatDesc* descs, int count, cudaStream_t st) {
+    for (int done = 0; done < count;) {
+        const int left = count - done;
+        const int n = left < kUploadLarge ? left : kUploadLarge;
+        const cudaError_t e = n <= kUploadSmall ? upload_batch<kUploadSmall>(d_descs + done, descs + done, n, st)
+                                                : upload_batch<kUploadLarge>(d_descs + done, descs + done, n, st);
+        if (e != cudaSuccess) return e;
+        done += n;
+    }
+    return cudaSuccess;
+}
 
 // max_tiles: largest ntiles over the wide matrices; tall_bf16 / tall_f32:
 // largest nparts over the tall matrices with bf16 / fp32 gradients (0 when

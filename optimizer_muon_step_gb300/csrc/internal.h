@@ -77,6 +77,17 @@ struct AdamwScalars {
 // launches and, when timing is enabled, record CUDA events on the stream.
 void launch_begin(int kind, cudaStream_t st);
 void launch_end(int kind, cudaStream_t st);
+// Between capture_begin and capture_end the calling thread's launches go
+// into a graph: they are counted apart (capture_end returns the count) and
+// never timed.  count_replay adds a replayed graph's launches to the total.
+void capture_begin();
+int64_t capture_end();
+void count_replay(int64_t launches);
+
+// ---- per-matrix records (elementwise.cu) ----------------------------------
+// Writes descs[0..count) to d_descs on `st` through kernel parameters, so the
+// upload needs no host buffer that outlives the call (stream-capture safe).
+cudaError_t launch_desc_upload(MatDesc* d_descs, const MatDesc* descs, int count, cudaStream_t st);
 
 // ---- element-wise kernels (elementwise.cu) --------------------------------
 // Momentum pass: M updated, X0 = bf16(u) in the wide orientation (tall
@@ -141,5 +152,9 @@ cudaError_t launch_wait_probe(int* status, long long limit_ns, cudaStream_t st);
 
 cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, const float* coeffs,
                    int* status, int num_sms, cudaStream_t st);
+// Sets the NS kernels' attributes and queries the pair occupancy for the
+// current device now (ns_run otherwise does it on first use), e.g. before a
+// stream capture.
+cudaError_t ns_prepare_device();
 
 }  // namespace muon

@@ -1195,47 +1195,50 @@ int triangle_tiles(int tiles_m, int tiles_n) {
 
 int triangle_pair_tiles(int tiles_n) { return tiles_n * (tiles_n + 1) / 2; }
 
+// Kernel attributes and the pair occupancy of one stage kernel, set up once
+// per device (with that device current) and remembered.
 template <int MODE, bool kPair>
-cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first, float a, float b, float c,
-                         int* status, int num_sms, cudaStream_t st) {
-    // Kernel attributes and the pair occupancy, set up once per device (with
-    // that device current) and remembered.
+cudaError_t stage_setup(int* max_pairs) {
     constexpr int kMaxDevices = 64;
     static std::mutex setup_mu;
     static bool setup_done[kMaxDevices] = {};
     static cudaError_t setup_err[kMaxDevices] = {};
     static int setup_pairs[kMaxDevices] = {};
     int dev = 0;
-    cudaError_t attr_err = cudaGetDevice(&dev);
-    if (attr_err != cudaSuccess) return attr_err;
+    const cudaError_t dev_err = cudaGetDevice(&dev);
+    if (dev_err != cudaSuccess) return dev_err;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    int max_pairs = 0;
-    {
-        std::lock_guard<std::mutex> lock(setup_mu);
-        if (!setup_done[dev]) {
-            cudaError_t e;
-            int n = 0;
-            if (kPair) {
-                e = cudaFuncSetAttribute(ns_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PSMEM_BYTES);
-                if (e == cudaSuccess) {
-                    cudaLaunchConfig_t cfg = {};
-                    cfg.gridDim = dim3(2, 1, 1);
-                    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-                    cfg.dynamicSmemBytes = PSMEM_BYTES;
-                    e = cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel<MODE>, &cfg);
-                }
-            } else {
-                e = cudaFuncSetAttribute(ns_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
+    std::lock_guard<std::mutex> lock(setup_mu);
+    if (!setup_done[dev]) {
+        cudaError_t e;
+        int n = 0;
+        if (kPair) {
+            e = cudaFuncSetAttribute(ns_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     PSMEM_BYTES);
+            if (e == cudaSuccess) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(2, 1, 1);
+                cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+                cfg.dynamicSmemBytes = PSMEM_BYTES;
+                e = cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel<MODE>, &cfg);
             }
-            setup_err[dev] = e;
-            setup_pairs[dev] = n;
-            setup_done[dev] = true;
+        } else {
+            e = cudaFuncSetAttribute(ns_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES);
         }
-        attr_err = setup_err[dev];
-        max_pairs = setup_pairs[dev];
+        setup_err[dev] = e;
+        setup_pairs[dev] = n;
+        setup_done[dev] = true;
     }
+    *max_pairs = setup_pairs[dev];
+    return setup_err[dev];
+}
+
+template <int MODE, bool kPair>
+cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first, float a, float b, float c,
+                         int* status, int num_sms, cudaStream_t st) {
+    int max_pairs = 0;
+    const cudaError_t attr_err = stage_setup<MODE, kPair>(&max_pairs);
     if (attr_err != cudaSuccess) return attr_err;
 
     NsParams prm;
@@ -1372,6 +1375,17 @@ cudaError_t ns_run(const NsGroup* groups, int ngroups, int steps, const float* c
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t ns_prepare_device() {
+    int n = 0;
+    cudaError_t e = stage_setup<MODE_SYRK, true>(&n);
+    if (e == cudaSuccess) e = stage_setup<MODE_POLY, true>(&n);
+    if (e == cudaSuccess) e = stage_setup<MODE_UPDATE, true>(&n);
+    if (e == cudaSuccess) e = stage_setup<MODE_SYRK, false>(&n);
+    if (e == cudaSuccess) e = stage_setup<MODE_POLY, false>(&n);
+    if (e == cudaSuccess) e = stage_setup<MODE_UPDATE, false>(&n);
+    return e;
 }
 
 }  // namespace muon

@@ -19,6 +19,8 @@ std::mutex g_mu;
 std::vector<Record> g_records;
 std::vector<cudaEvent_t> g_pool;
 Record g_open{-1, nullptr, nullptr};
+// launches the calling thread made since its capture_begin; -1 outside a capture
+thread_local int64_t t_captured = -1;
 
 cudaEvent_t take_event() {
     if (!g_pool.empty()) {
@@ -42,6 +44,10 @@ void drop_records_locked() {
 }  // namespace
 
 void launch_begin(int kind, cudaStream_t st) {
+    if (t_captured >= 0) {
+        ++t_captured;
+        return;
+    }
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (!g_enabled.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -52,13 +58,23 @@ void launch_begin(int kind, cudaStream_t st) {
 }
 
 void launch_end(int kind, cudaStream_t st) {
-    if (!g_enabled.load(std::memory_order_relaxed)) return;
+    if (t_captured >= 0 || !g_enabled.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_open.kind != kind || !g_open.start || !g_open.stop) return;
     cudaEventRecord(g_open.stop, st);
     g_records.push_back(g_open);
     g_open = Record{-1, nullptr, nullptr};
 }
+
+void capture_begin() { t_captured = 0; }
+
+int64_t capture_end() {
+    const int64_t n = t_captured < 0 ? 0 : t_captured;
+    t_captured = -1;
+    return n;
+}
+
+void count_replay(int64_t launches) { g_launches.fetch_add(launches, std::memory_order_relaxed); }
 
 }  // namespace muon
 
@@ -113,6 +129,7 @@ const char* muon_kernel_name(int32_t kind) {
         case MUON_KERNEL_FINAL_UPDATE: return "final_update";
         case MUON_KERNEL_ADAMW: return "adamw";
         case MUON_KERNEL_GRAD_GUARD: return "grad_guard";
+        case MUON_KERNEL_DESC_UPLOAD: return "desc_upload";
     }
     return "unknown";
 }

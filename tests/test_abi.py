@@ -194,6 +194,51 @@ def test_bounded_wait_check_validation(built):
     assert built.muon_check_bounded_wait(P(4100), 1000, None) == 3
 
 
+def test_graph_argument_validation(built):
+    lib = built
+    P = ctypes.c_void_p
+    arr = (m.MuonMatrix * 1)()
+    arr[0].W = arr[0].G = arr[0].M = 1024
+    arr[0].rows, arr[0].cols = 4, 4
+    out = P(12345)
+    # no output handle
+    assert lib.muon_step_graph_create(arr, 1, ctypes.byref(_hp()), P(4096), 1 << 20, None) == 1
+    # the step's own checks, before anything is captured; the handle is cleared
+    bad = _hp()
+    bad.momentum = -0.5
+    assert lib.muon_step_graph_create(arr, 1, ctypes.byref(bad), P(4096), 1 << 20, ctypes.byref(out)) == 1
+    assert out.value is None
+    arr[0].g_dtype = 7
+    assert lib.muon_step_graph_create(arr, 1, ctypes.byref(_hp()), P(4096), 1 << 20, ctypes.byref(out)) == 2
+    arr[0].g_dtype = 0
+    assert lib.muon_step_graph_create(arr, 1, ctypes.byref(_hp()), P(4100), 1 << 20, ctypes.byref(out)) == 3
+    assert lib.muon_step_graph_create(arr, 1, ctypes.byref(_hp()), None, 1 << 20, ctypes.byref(out)) == 1
+    # launch of no graph; destroy of none is a no-op
+    assert lib.muon_step_graph_launch(None, None) == 1
+    assert lib.muon_step_graph_destroy(None) == 0
+
+
+def test_graph_of_no_matrices_is_a_no_op(built):
+    lib = built
+    out = ctypes.c_void_p()
+    assert lib.muon_step_graph_create(None, 0, ctypes.byref(_hp()), None, 0, ctypes.byref(out)) == 0
+    assert out.value is not None
+    assert lib.muon_step_graph_launch(out, None) == 0
+    assert lib.muon_step_graph_destroy(out) == 0
+
+
+@pytest.mark.skipif(cuda_available(), reason="checks the no-device path")
+def test_graph_without_device_reports_no_device(built):
+    arr = (m.MuonMatrix * 1)()
+    arr[0].W = arr[0].G = arr[0].M = 1024
+    arr[0].rows, arr[0].cols = 4, 4
+    out = ctypes.c_void_p(12345)
+    st = built.muon_step_graph_create(arr, 1, ctypes.byref(_hp()), ctypes.c_void_p(4096), 1 << 20,
+                                      ctypes.byref(out))
+    assert st == 7
+    assert out.value is None
+
+
 def test_library_never_loads_the_oracle(built):
     # the product path has no reference to the oracle
     for path in ("optimizer_muon_step_gb300/__init__.py", "optimizer_muon_step_gb300/build.py"):
