@@ -20,6 +20,9 @@ scaling, no collective on the data path).  The default workload's inputs
 total > 12 GB, far larger than L2 (129 MB); a workload whose W, G and M fit
 in 4 x L2 has L2 flushed between timed steps instead (a 512 MB write outside
 the per-step events).
+
+graph_replay: the same step captured once as a CUDA graph
+(muon_step_graph_create) and replayed; each replay timed on its own.
 """
 from __future__ import annotations
 
