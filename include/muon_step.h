@@ -149,8 +149,9 @@ muon_status_t muon_plan(const muon_matrix_t* mats, int64_t count,
  * count == 0 is a no-op.  A kernel that gives up on a bounded wait records
  * MUON_ERR_TIMEOUT in the workspace; read it with muon_query_status.
  * The call enqueues kernels and one memset only (no host<->device copy, no
- * synchronisation), so it may run inside a CUDA stream capture; see
- * muon_step_graph_create. */
+ * synchronisation), so it may run inside a CUDA stream capture once one
+ * call has run on the device outside a capture (the first call sets kernel
+ * attributes); muon_step_graph_create needs no such call. */
 muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count,
                                 const muon_hparams_t* hp, void* workspace,
                                 size_t ws_bytes, void* stream);
