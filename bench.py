@@ -22,7 +22,9 @@ in 4 x L2 has L2 flushed between timed steps instead (a 512 MB write outside
 the per-step events).
 
 graph_replay: the same step captured once as a CUDA graph
-(muon_step_graph_create) and replayed; each replay timed on its own.
+(muon_step_graph_create) and replayed, each replay timed on its own and
+alternating with eager steps (no per-launch timing events), whose median is
+reported beside it.
 """
 from __future__ import annotations
 
@@ -577,7 +579,8 @@ def run_ours(args, rank, world, local_rank):
                  "guard_gbs": g_bytes / (guard_ms / 1e3) / 1e9, "guard_bytes_per_step": g_bytes,
                  "settings": "skip_nonfinite=1, max_grad_norm=1e9"}
 
-    # ---- the same step replayed from a captured CUDA graph ----
+    # ---- the same step replayed from a captured CUDA graph, alternating
+    # with eager calls so both see the same clocks ----
     graph = None
     if not args.no_graph:
         g = batch.capture(hp)
@@ -585,25 +588,33 @@ def run_ours(args, rank, world, local_rank):
             g.launch(stream)
         torch.cuda.synchronize()
         n_graph = max(3, min(args.steps, 20))
-        g_events = []
+        ev = {"graph": [], "eager": []}
         gl0 = m.muon_launch_count()
         for _ in range(n_graph):
-            if flush is not None:
-                with torch.cuda.stream(stream):
-                    flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g.launch(stream)
-            b.record(stream)
-            g_events.append((a, b))
+            for kind in ("eager", "graph"):
+                if flush is not None:
+                    with torch.cuda.stream(stream):
+                        flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                if kind == "graph":
+                    g.launch(stream)
+                else:
+                    batch.step(hp, stream)
+                b.record(stream)
+                ev[kind].append((a, b))
         torch.cuda.synchronize()
+        n_launch = (m.muon_launch_count() - gl0) / (2 * n_graph)
         g.destroy()
         if m.muon_query_status(batch.workspace) != 0:
             raise RuntimeError("device status set in the graph replays")
-        g_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in g_events)) / n_graph
+        g_times = [a.elapsed_time(b) for a, b in ev["graph"]]
+        e_times = [a.elapsed_time(b) for a, b in ev["eager"]]
+        g_ms = max_over_ranks(sum(g_times)) / n_graph
         graph = {"ms_per_step": g_ms, "value": aggregate_tflops(step_flops, n_graph, world, g_ms * n_graph),
-                 "steps": n_graph, "launches_per_step": (m.muon_launch_count() - gl0) / n_graph,
-                 "timed": "per replay, CUDA events around each graph launch"
+                 "median_ms": statistics.median(g_times), "eager_median_ms": statistics.median(e_times),
+                 "steps": n_graph, "launches_per_step": n_launch,
+                 "timed": "per call, CUDA events around each graph launch and each eager step, alternating"
                           + ("; L2 flushed before each" if flush is not None else "")}
 
     # ---- end to end through the public API, host buffers ----
