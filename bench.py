@@ -48,7 +48,7 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 << 20  # GB300 L2
 ADAMW_BYTES_PER_PARAM = 28  # read p, g, m, v (16 B), write p, m, v (12 B)
 KINDS = ("momentum_norm", "norm_finalize", "x0_rescale", "ns_syrk", "ns_poly", "ns_update",
-         "final_update", "adamw", "grad_guard", "desc_upload")
+         "final_update", "adamw", "grad_guard", "desc_upload", "stats")
 
 
 def parse():

@@ -156,6 +156,32 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count,
                                 const muon_hparams_t* hp, void* workspace,
                                 size_t ws_bytes, void* stream);
 
+/* Per-matrix statistics of one step (no counterpart in the update itself;
+ * the pages suggest watching such quantities, [OPT] section 5).  fp64:
+ *   u_norm      ||u||_F, the Frobenius norm of the look-ahead the step
+ *               normalised: sqrt of the sum of the momentum pass's fp32
+ *               tile sums of u^2, summed in fp64
+ *   update_rms  sqrt(sum fl(scale * O)^2 / (rows * cols)), the RMS of the
+ *               RMS-matched update before lr and decay ([K2] section 3.1:
+ *               about 0.2, in AdamW's 0.2-0.4 band, with scale_mode 0);
+ *               each square in fp32, tile sums in fp32, summed in fp64
+ * Both are NaN for every matrix when the non-finite guard skipped the step. */
+typedef struct {
+    double u_norm;
+    double update_rms;
+} muon_matrix_stats_t;
+
+/* muon_step_batched plus per-matrix statistics: `stats` is device memory of
+ * `count` entries, 8-byte aligned, entry i for mats[i], written on `stream`
+ * during the step.  Costs one extra read of each matrix's NS output (2 bytes
+ * per element) and two launches per workspace chunk.  Same arguments,
+ * checks and errors as muon_step_batched; a null `stats` is
+ * MUON_ERR_INVALID_ARG, a misaligned one MUON_ERR_MISALIGNED. */
+muon_status_t muon_step_batched_stats(const muon_matrix_t* mats, int64_t count,
+                                      const muon_hparams_t* hp, void* workspace,
+                                      size_t ws_bytes, muon_matrix_stats_t* stats,
+                                      void* stream);
+
 /* Size of the library-owned device scratch used by muon_step_batched_noalloc:
  * 64 MiB on every GPU where the library's device code is loaded, held until
  * the process exits. */
@@ -277,7 +303,8 @@ typedef enum {
     MUON_KERNEL_ADAMW = 7,          /* AdamW                                */
     MUON_KERNEL_GRAD_GUARD = 8,     /* global gradient norm / non-finite    */
     MUON_KERNEL_DESC_UPLOAD = 9,    /* per-matrix records into the workspace */
-    MUON_KERNEL_COUNT = 10
+    MUON_KERNEL_STATS = 10,         /* per-matrix step statistics           */
+    MUON_KERNEL_COUNT = 11
 } muon_kernel_kind_t;
 
 /* Process-wide count of kernels this library has launched (all kinds); a

@@ -43,9 +43,9 @@ EXPORTS = ("muon_workspace_bytes_per_matrix", "muon_workspace_size", "muon_plan"
            "muon_status_string", "muon_version", "muon_launch_count", "muon_set_timing",
            "muon_timing_read", "muon_kernel_name", "muon_step_batched_noalloc",
            "muon_check_bounded_wait", "muon_step_graph_create", "muon_step_graph_launch",
-           "muon_step_graph_destroy")
+           "muon_step_graph_destroy", "muon_step_batched_stats")
 KERNEL_KINDS = ("momentum_norm", "norm_finalize", "x0_rescale", "ns_syrk", "ns_poly",
-                "ns_update", "final_update", "adamw", "grad_guard", "desc_upload")
+                "ns_update", "final_update", "adamw", "grad_guard", "desc_upload", "stats")
 
 
 class MuonError(RuntimeError):
@@ -158,6 +158,8 @@ def load_library(path: str = LIB_PATH):
         lib.muon_plan.restype = ctypes.c_int
         lib.muon_step_batched.argtypes = [P, i64, P, P, ctypes.c_size_t, P]
         lib.muon_step_batched.restype = ctypes.c_int
+        lib.muon_step_batched_stats.argtypes = [P, i64, P, P, ctypes.c_size_t, P, P]
+        lib.muon_step_batched_stats.restype = ctypes.c_int
         lib.muon_step_batched_noalloc.argtypes = [P, i64, P, P]
         lib.muon_step_batched_noalloc.restype = ctypes.c_int
         lib.muon_newton_schulz.argtypes = [P, P, i64, i64, i64, i32, P, i32, P, ctypes.c_size_t, P]
@@ -256,12 +258,22 @@ def allocate_workspace(nbytes: int, device=None):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
 
 
+def _stats_tensor(stats, n):
+    import torch
+    if not (isinstance(stats, torch.Tensor) and stats.is_cuda and stats.dtype == torch.float64
+            and stats.is_contiguous() and tuple(stats.shape) == (n, 2)):
+        raise ValueError(f"stats must be a contiguous CUDA float64 tensor of shape ({n}, 2)")
+    return ctypes.c_void_p(stats.data_ptr())
+
+
 def muon_step_batched(W, G, M, hp: MuonHparams = MuonHparams(), workspace=None, stream=None,
-                      budget_bytes: int = 16 << 30):
+                      budget_bytes: int = 16 << 30, stats=None):
     """One Muon step on lists of matrices (in place on every W and M).
 
     W, M: fp32 CUDA tensors (rows x cols); G: fp32 or bf16 of the same shape.
     workspace: a uint8 CUDA tensor; allocated here (torch) when None.
+    stats: optional CUDA float64 tensor (len(W), 2) that receives each
+    matrix's (||u||_F, update RMS) (muon_step_batched_stats).
     Returns the workspace so callers can reuse it."""
     import torch
     n = len(W)
@@ -284,9 +296,15 @@ def muon_step_batched(W, G, M, hp: MuonHparams = MuonHparams(), workspace=None, 
                                        ctypes.byref(need)), "muon_workspace_size")
         workspace = allocate_workspace(need.value, W[0].device if n else None)
     h = hp._c()
-    _check(lib.muon_step_batched(ctypes.cast(arr, ctypes.c_void_p), n, ctypes.byref(h),
-                                 ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
-                                 _stream(stream)), "muon_step_batched")
+    if stats is None:
+        _check(lib.muon_step_batched(ctypes.cast(arr, ctypes.c_void_p), n, ctypes.byref(h),
+                                     ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                     _stream(stream)), "muon_step_batched")
+    else:
+        _check(lib.muon_step_batched_stats(ctypes.cast(arr, ctypes.c_void_p), n, ctypes.byref(h),
+                                           ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                           _stats_tensor(stats, n), _stream(stream)),
+               "muon_step_batched_stats")
     return workspace
 
 
@@ -434,6 +452,21 @@ class MuonBatch:
                                                 ctypes.c_void_p(self.workspace.data_ptr()),
                                                 self.workspace.numel(), _stream(stream)),
                "muon_step_batched")
+
+    def step_with_stats(self, hp: MuonHparams = MuonHparams(), stream=None, out=None):
+        """The step plus each matrix's (||u||_F, update RMS): returns a CUDA
+        float64 tensor (count, 2), `out` when given (muon_step_batched_stats)."""
+        import torch
+        if out is None:
+            out = torch.empty((self.count, 2), dtype=torch.float64, device=self.workspace.device)
+        h = hp._c()
+        _check(load_library().muon_step_batched_stats(ctypes.cast(self.arr, ctypes.c_void_p), self.count,
+                                                      ctypes.byref(h),
+                                                      ctypes.c_void_p(self.workspace.data_ptr()),
+                                                      self.workspace.numel(), _stats_tensor(out, self.count),
+                                                      _stream(stream)),
+               "muon_step_batched_stats")
+        return out
 
     def capture(self, hp: MuonHparams = MuonHparams()) -> "MuonGraph":
         """The step with these hyper-parameters captured once as a CUDA

@@ -7,6 +7,7 @@
 //   [0, 256)                 WsHeader: status word, gradient-guard results
 //   [256, ...)               MatDesc[n]
 //   [.., +n*4096)            norm partial sums, 1024 floats per matrix
+//   [.., +n*2048)            statistics pass sums, 512 floats per matrix
 //   [n*8192, ...)            per shape group of c matrices:
 //                              X0[c], X1[c]  (each R(2 m' L(n')) bytes)
 //                              A[c],  B[c]   (each R(2 m' L(m')) bytes)
@@ -286,8 +287,13 @@ muon_status_t muon_plan(const muon_matrix_t* mats, int64_t count, size_t ws_byte
     return MUON_OK;
 }
 
-muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const muon_hparams_t* hp,
-                                void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The step, with per-matrix statistics when `stats` is non-null.
+muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hparams_t* hp, void* workspace,
+                        size_t ws_bytes, muon_matrix_stats_t* stats, void* stream) {
     muon_status_t s = check_hparams(hp);
     if (s != MUON_OK) return s;
     s = check_shapes(mats, count);
@@ -325,6 +331,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
     int max_units = 0;       // tall-pass units (momentum pass)
     int64_t max_final_units = 0;  // tall units of the final update
     int tall_units[2] = {0, 0};  // the same, over tall matrices with fp32 / bf16 gradients
+    float* o_partials = nullptr;  // statistics pass: kStatsTiles sums per matrix after the norm partials
 
     // Fills `descs` and the layout for plan rows [b, e) and uploads them (by
     // kernel parameters: no host buffer outlives the call, so the sequence
@@ -334,6 +341,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
         layout_groups(plan, b, e, ws, L);
         float* d_partials = reinterpret_cast<float*>(
             ws + kHeaderBytes + round_up(static_cast<int64_t>(n) * static_cast<int64_t>(sizeof(MatDesc)), 256));
+        o_partials = d_partials + static_cast<int64_t>(n) * kMaxNormTiles;
         descs.assign(n, MatDesc{});
         max_tiles = 1;
         max_wide_tiles = max_units = 0;
@@ -367,6 +375,7 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
                       reinterpret_cast<uintptr_t>(m.M)) & 15u) == 0 ? 1 : 0;
             d.scale = 0.f;
             d.update_scale = update_scale(hp, m.rows, m.cols);
+            d.stats = stats ? stats + row.idx : nullptr;
             if (d.transposed) {
                 // units of tall_kc x tall_kr 64x64 tiles, at most kMaxNormTiles
                 const int64_t rt = (m.rows + 63) / 64, ct = (m.cols + 63) / 64;
@@ -435,8 +444,28 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const 
         if (s != MUON_OK) return s;
         s = from_cuda(launch_final_update(d_descs, n, max_wide_tiles, max_final_units, us, st));
         if (s != MUON_OK) return s;
+        if (stats) {
+            s = from_cuda(launch_step_stats(d_descs, n, o_partials, guard_on ? header : nullptr, st));
+            if (s != MUON_OK) return s;
+        }
     }
     return MUON_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count, const muon_hparams_t* hp,
+                                void* workspace, size_t ws_bytes, void* stream) {
+    return step_impl(mats, count, hp, workspace, ws_bytes, nullptr, stream);
+}
+
+muon_status_t muon_step_batched_stats(const muon_matrix_t* mats, int64_t count, const muon_hparams_t* hp,
+                                      void* workspace, size_t ws_bytes, muon_matrix_stats_t* stats, void* stream) {
+    if (!stats) return MUON_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(stats) & 7u) return MUON_ERR_MISALIGNED;
+    return step_impl(mats, count, hp, workspace, ws_bytes, stats, stream);
 }
 
 }  // extern "C"

@@ -35,14 +35,17 @@ struct MatDesc {
     float rescale_factor;
     float ns_scale;      // factor the first NS step applies to X0
     double gsum;         // gradient guard: sum of G^2 over the matrix (fp64)
+    muon_matrix_stats_t* stats;  // this matrix's statistics entry (device), or null
 };
 
 constexpr int kMaxNormTiles = 1024;
+constexpr int kStatsTiles = 512;          // row tiles of the statistics pass per matrix
 constexpr size_t kRecordBytes = 8192;     // per matrix, see muon_step.h
 constexpr size_t kHeaderBytes = 256;
 // a matrix's record and partials fit its kRecordBytes (header and rounding
 // covered by the slack); the NS kernels index ns_scale in float strides
-static_assert(sizeof(MatDesc) + sizeof(float) * kMaxNormTiles + 512 <= kRecordBytes, "record overflow");
+static_assert(sizeof(MatDesc) + sizeof(float) * (kMaxNormTiles + kStatsTiles) + 512 <= kRecordBytes,
+              "record overflow");
 static_assert(sizeof(MatDesc) % sizeof(float) == 0, "record stride");
 
 // Start of the workspace: status word and the gradient guard's results.
@@ -120,6 +123,14 @@ cudaError_t launch_grad_stats(const MatDesc* descs, int count, int max_tiles, Ws
 cudaError_t launch_grad_stats_reduce(MatDesc* descs, int count, WsHeader* header, cudaStream_t st);
 cudaError_t launch_grad_decide(WsHeader* header, float max_grad_norm, int32_t skip_nonfinite,
                                cudaStream_t st);
+
+// ---- step statistics (stats.cu) ------------------------------------------
+// For every matrix with a stats entry: the RMS of scale * O over row tiles
+// into o_partials (kStatsTiles floats per matrix), then ||u||_F from the
+// norm partials and the update RMS into the entry (NaN when the guard's
+// skip flag is set in `header`; header may be null).
+cudaError_t launch_step_stats(const MatDesc* descs, int count, float* o_partials, const WsHeader* header,
+                              cudaStream_t st);
 
 // ---- Newton-Schulz GEMMs (ns_gemm.cu) -------------------------------------
 // One shape group of wide bf16 matrices in the workspace: `count` matrices,

@@ -130,6 +130,7 @@ const char* muon_kernel_name(int32_t kind) {
         case MUON_KERNEL_ADAMW: return "adamw";
         case MUON_KERNEL_GRAD_GUARD: return "grad_guard";
         case MUON_KERNEL_DESC_UPLOAD: return "desc_upload";
+        case MUON_KERNEL_STATS: return "stats";
     }
     return "unknown";
 }

@@ -90,6 +90,8 @@ def _load():
             lib.oracle_final_update.argtypes = [P, P, i64, i64, ctypes.c_float, ctypes.c_float,
                                                 ctypes.c_float, ctypes.c_int]
             lib.oracle_final_update.restype = None
+            lib.oracle_step_stats.argtypes = [P, P, i64, i64, ctypes.c_float, ctypes.c_int, P, P]
+            lib.oracle_step_stats.restype = None
             lib.oracle_muon_step_matrix.argtypes = [P, P, P, i64, i64, P, P, P]
             lib.oracle_muon_step_matrix.restype = ctypes.c_int
             lib.oracle_muon_step_matrix_scaled.argtypes = [P, P, P, i64, i64, P, ctypes.c_float,
@@ -281,6 +283,21 @@ def final_update(W, O, lr=0.02, weight_decay=0.1, rms_scale=0.2, scale_mode=0):
     _load().oracle_final_update(_ptr(W), _ptr(O), rows, cols, float(lr), float(weight_decay),
                                 float(rms_scale), int(scale_mode))
     return W
+
+
+def step_stats(u, O, rms_scale=0.2, scale_mode=0):
+    """(||u||_F, update RMS) of one matrix: u the look-ahead (rows x cols),
+    O the wide NS output; the update RMS is that of fl(scale * O)."""
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    O = np.ascontiguousarray(O, dtype=np.float32)
+    rows, cols = u.shape
+    if O.shape != (min(rows, cols), max(rows, cols)):
+        raise ValueError("O must be the wide (min x max) NS output")
+    un = ctypes.c_double(0.0)
+    ur = ctypes.c_double(0.0)
+    _load().oracle_step_stats(_ptr(u), _ptr(O), rows, cols, float(rms_scale), int(scale_mode),
+                              ctypes.byref(un), ctypes.byref(ur))
+    return float(un.value), float(ur.value)
 
 
 def grad_stats(Gs):

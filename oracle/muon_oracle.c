@@ -340,6 +340,32 @@ void oracle_final_update(float* W, const float* O, int64_t rows, int64_t cols,
         }
 }
 
+/* Per-matrix statistics of a step, for monitoring (the update does not use
+ * them):
+ *   u_norm     = sqrt(sum u^2), the fp64 sum in element order: the norm that
+ *                step 3 divides by
+ *   update_rms = sqrt(sum fl(scale * o)^2 / (rows * cols)): each product and
+ *                square rounded to fp32, summed in fp64; scale as in step 7.
+ *                This is the RMS of the RMS-matched update before lr and
+ *                decay, which [K2] section 3.1 sets to match AdamW's 0.2-0.4.
+ * u: rows x cols; O: the wide NS output (min x max), rows * cols values. */
+void oracle_step_stats(const float* u, const float* O, int64_t rows, int64_t cols,
+                       float rms_scale, int scale_mode, double* u_norm, double* update_rms)
+{
+    const int64_t n = rows * cols;
+    double su = 0.0, so = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        su += (double)u[i] * (double)u[i];
+    const float scale = oracle_update_scale(rows, cols, rms_scale, scale_mode);
+    for (int64_t i = 0; i < n; ++i) {
+        const float v = scale * O[i];
+        const float sq = v * v;
+        so += (double)sq;
+    }
+    *u_norm = sqrt(su);
+    *update_rms = sqrt(so / (double)n);
+}
+
 /* One Muon step on one rows x cols matrix, in place on W and M:
  * oracle_momentum (on g_scale * G when scale_g != 0), oracle_normalize, NS
  * (bf16 emulation; per-step coefficients when hp->ns_coeffs is set) on the

@@ -194,6 +194,24 @@ def test_bounded_wait_check_validation(built):
     assert built.muon_check_bounded_wait(P(4100), 1000, None) == 3
 
 
+def test_stats_argument_validation(built):
+    lib = built
+    P = ctypes.c_void_p
+    arr = (m.MuonMatrix * 1)()
+    arr[0].W = arr[0].G = arr[0].M = 1024
+    arr[0].rows, arr[0].cols = 4, 4
+    # no statistics buffer, a misaligned one; then the step's own checks
+    assert lib.muon_step_batched_stats(arr, 1, ctypes.byref(_hp()), P(4096), 1 << 20, None, None) == 1
+    assert lib.muon_step_batched_stats(arr, 1, ctypes.byref(_hp()), P(4096), 1 << 20, P(8196), None) == 3
+    bad = _hp()
+    bad.ns_steps = 101
+    assert lib.muon_step_batched_stats(arr, 1, ctypes.byref(bad), P(4096), 1 << 20, P(8192), None) == 1
+    arr[0].W = 1026
+    assert lib.muon_step_batched_stats(arr, 1, ctypes.byref(_hp()), P(4096), 1 << 20, P(8192), None) == 3
+    # no matrices: a no-op
+    assert lib.muon_step_batched_stats(None, 0, ctypes.byref(_hp()), None, 0, P(8192), None) == 0
+
+
 def test_graph_argument_validation(built):
     lib = built
     P = ctypes.c_void_p

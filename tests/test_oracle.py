@@ -527,3 +527,54 @@ def test_grad_clip_inactive_below_threshold_and_direction_only_above():
     for (W1, M1), (W2, M2) in zip(one, two):
         assert np.allclose(M1, M2, rtol=1e-6, atol=0)
         assert np.allclose(W1, W2, rtol=1e-6, atol=1e-9)
+
+
+# ---- per-matrix step statistics (monitoring output) -------------------------
+
+def test_step_stats_u_norm_is_the_frobenius_norm():
+    """u_norm is ||u||_F: numpy's norm of the fp64 widening, a separate route."""
+    rng = np.random.default_rng(11)
+    for rows, cols in ((37, 53), (90, 20)):
+        u = (rng.standard_normal((rows, cols)) * 1e-2).astype(np.float32)
+        O = np.zeros((min(rows, cols), max(rows, cols)), np.float32)
+        un, _ = oracle.step_stats(u, O)
+        assert abs(un / np.linalg.norm(u.astype(np.float64)) - 1) < 1e-12
+
+
+@pytest.mark.parametrize("rows,cols", [(48, 112), (112, 48)])
+def test_step_stats_update_rms_of_orthonormal_rows(rows, cols):
+    """An O with orthonormal rows ([I 0], every singular value 1) has
+    ||O||_F^2 = m', so the RMS of scale * O over the m*n entries is
+    scale * sqrt(m' / (m n)) = 0.2 sqrt(n') / sqrt(n') = 0.2: the update RMS
+    the RMS matching of [K2] section 3.1 targets."""
+    mp, np_ = min(rows, cols), max(rows, cols)
+    O = np.zeros((mp, np_), np.float32)
+    O[:, :mp] = np.eye(mp, dtype=np.float32)
+    u = np.ones((rows, cols), np.float32)
+    _, rms = oracle.step_stats(u, O)
+    # each scaled square is rounded to fp32: within one fp32 rounding (2^-24)
+    scale = float(np.float32(0.2 * math.sqrt(np_)))
+    assert abs(rms / (scale * math.sqrt(mp / (rows * cols))) - 1) < 2.0 ** -24
+    assert abs(rms - 0.2) < 1e-7
+    # muP-style scale: max(1, sqrt(rows / cols)) * sqrt(m' / (m n))
+    _, rms1 = oracle.step_stats(u, O, scale_mode=1)
+    s1 = float(np.float32(max(1.0, math.sqrt(rows / cols))))
+    assert abs(rms1 / (s1 * math.sqrt(mp / (rows * cols))) - 1) < 2.0 ** -24
+
+
+def test_step_stats_update_rms_from_singular_values():
+    """For a real NS output, ||O||_F^2 = sum sigma_i^2 (from an SVD, not the
+    element sum), so update_rms = scale * sqrt(sum sigma^2 / (m n)) up to the
+    fp32 rounding of each scaled element; and it lies in the 0.2-0.4 band of
+    [K2] section 3.1 (low end: the quintic leaves sigma in about [0.7, 1.2])."""
+    for rows, cols in ((64, 160), (160, 64)):
+        W, G, M = _inputs(rows, cols, 7)
+        hp = oracle.MuonConfig()
+        _, u = oracle.momentum(G, M, hp.momentum, hp.nesterov)
+        _, _, _, O = oracle.muon_step_matrix(W, G, M, hp)
+        _, rms = oracle.step_stats(u, O)
+        sig = np.linalg.svd(O.astype(np.float64), compute_uv=False)
+        scale = float(np.float32(0.2 * math.sqrt(max(rows, cols))))
+        expected = scale * math.sqrt(np.sum(sig ** 2) / (rows * cols))
+        assert abs(rms / expected - 1) < 1e-6
+        assert 0.14 < rms < 0.4
