@@ -66,8 +66,9 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
         list(ex.map(run, jobs))
     if jobs or _newer(LIB_PATH, objs):
         tmp = LIB_PATH + f".tmp{os.getpid()}"
+        # -ldl: the header-only NVTX looks up an attached tool with dlopen
         run([nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-             "-Xlinker", f"-rpath,{cuda_lib_dir()}"])
+             "-Xlinker", f"-rpath,{cuda_lib_dir()}", "-ldl"])
         os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

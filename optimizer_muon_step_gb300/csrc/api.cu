@@ -294,6 +294,7 @@ namespace {
 // The step, with per-matrix statistics when `stats` is non-null.
 muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hparams_t* hp, void* workspace,
                         size_t ws_bytes, muon_matrix_stats_t* stats, void* stream) {
+    NvtxScope range("muon_step");
     muon_status_t s = check_hparams(hp);
     if (s != MUON_OK) return s;
     s = check_shapes(mats, count);
@@ -428,6 +429,7 @@ muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hpa
     }
 
     for (size_t ci = 0; ci < chunks.size(); ++ci) {
+        NvtxScope chunk_range("muon_step chunk");
         const size_t b = chunks[ci].first, e = chunks[ci].second;
         const int n = static_cast<int>(e - b);
         if (!(guard_on && chunks.size() == 1)) {  // a single chunk is still in place from the guard
@@ -480,6 +482,7 @@ extern "C" {
 
 muon_status_t muon_step_graph_create(const muon_matrix_t* mats, int64_t count, const muon_hparams_t* hp,
                                      void* workspace, size_t ws_bytes, muon_graph_t* out) {
+    NvtxScope range("muon_step_graph_create");
     if (!out) return MUON_ERR_INVALID_ARG;
     *out = nullptr;
     // the host-side checks of the step, so that a bad call captures nothing
@@ -541,6 +544,7 @@ muon_status_t muon_step_graph_destroy(muon_graph_t graph) {
 muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t count, int64_t mp, int64_t np,
                                  int32_t ns_steps, const float* coeff_in, int32_t ncoeff_sets, void* workspace,
                                  size_t ws_bytes, void* stream) {
+    NvtxScope range("muon_newton_schulz");
     if (count < 0 || mp <= 0 || np <= 0 || mp > np || ns_steps < 0 || ns_steps > 100) return MUON_ERR_INVALID_ARG;
     if (np > (int64_t(1) << 30)) return MUON_ERR_INVALID_ARG;
     if (ns_steps > 0 && (!coeff_in || (ncoeff_sets != 1 && ncoeff_sets != ns_steps))) return MUON_ERR_INVALID_ARG;
@@ -605,6 +609,7 @@ muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t 
 
 muon_status_t adamw_step(float* p, const float* g, float* m, float* v, int64_t n, const adamw_hparams_t* hp,
                          int64_t step, void* stream) {
+    NvtxScope range("adamw_step");
     if (!hp || n < 0 || step < 1) return MUON_ERR_INVALID_ARG;
     if (!finite(hp->lr) || !finite(hp->beta1) || !finite(hp->beta2) || !finite(hp->eps) ||
         !finite(hp->weight_decay))

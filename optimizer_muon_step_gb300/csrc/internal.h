@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -77,7 +78,11 @@ struct AdamwScalars {
 
 // ---- launch accounting (timing.cu) -----------------------------------------
 // Every kernel launch is bracketed by launch_begin / launch_end: they count
-// launches and, when timing is enabled, record CUDA events on the stream.
+// launches, open and close an NVTX range named for the kernel kind, and,
+// when timing is enabled, record CUDA events on the stream.  With the
+// environment variable MUON_DEBUG set to a nonzero value, launch_end also
+// synchronises the stream (unless it is being captured) and reports a
+// failed kernel by name on stderr.
 void launch_begin(int kind, cudaStream_t st);
 void launch_end(int kind, cudaStream_t st);
 // Between capture_begin and capture_end the calling thread's launches go
@@ -86,6 +91,14 @@ void launch_end(int kind, cudaStream_t st);
 void capture_begin();
 int64_t capture_end();
 void count_replay(int64_t launches);
+
+// An NVTX range over a scope of host code (an API call).
+struct NvtxScope {
+    explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+    ~NvtxScope() { nvtxRangePop(); }
+    NvtxScope(const NvtxScope&) = delete;
+    NvtxScope& operator=(const NvtxScope&) = delete;
+};
 
 // ---- per-matrix records (elementwise.cu) ----------------------------------
 // Writes descs[0..count) to d_descs on `st` through kernel parameters, so the

@@ -1,4 +1,7 @@
 // Launch counting and optional per-launch CUDA-event timing.
+#include <stdio.h>
+#include <stdlib.h>
+
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -41,6 +44,24 @@ void drop_records_locked() {
     g_records.clear();
 }
 
+// MUON_DEBUG, read once per process
+bool debug_mode() {
+    static const bool on = [] {
+        const char* v = getenv("MUON_DEBUG");
+        return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+    }();
+    return on;
+}
+
+// Debug mode: waits for the launch and reports it by name if it failed.
+void debug_check(int kind, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaPeekAtLastError();
+    if (e != cudaSuccess) fprintf(stderr, "muon: kernel %s failed: %s\n", muon_kernel_name(kind), cudaGetErrorString(e));
+}
+
 }  // namespace
 
 void launch_begin(int kind, cudaStream_t st) {
@@ -48,6 +69,7 @@ void launch_begin(int kind, cudaStream_t st) {
         ++t_captured;
         return;
     }
+    nvtxRangePushA(muon_kernel_name(kind));
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (!g_enabled.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -58,7 +80,10 @@ void launch_begin(int kind, cudaStream_t st) {
 }
 
 void launch_end(int kind, cudaStream_t st) {
-    if (t_captured >= 0 || !g_enabled.load(std::memory_order_relaxed)) return;
+    if (t_captured >= 0) return;
+    nvtxRangePop();
+    if (debug_mode()) debug_check(kind, st);
+    if (!g_enabled.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_open.kind != kind || !g_open.start || !g_open.stop) return;
     cudaEventRecord(g_open.stop, st);

@@ -43,3 +43,43 @@ def test_bounded_wait_argument_checks(lib):
     for bad in (0, -5, 10 ** 8):
         with pytest.raises(m.MuonError):
             m.muon_check_bounded_wait(ws, limit_us=bad)
+
+
+_DEBUG_SCRIPT = """
+import sys
+import torch
+sys.path.insert(0, sys.argv[2])
+import optimizer_muon_step_gb300 as m
+gen = torch.Generator(device="cuda").manual_seed(61)
+shapes = [(256, 512), (130, 70), (520, 256)]
+W = [torch.randn(r, c, device="cuda", generator=gen) * 0.02 for r, c in shapes]
+G = [torch.randn(r, c, device="cuda", generator=gen) * 1e-2 for r, c in shapes]
+M = [torch.randn(r, c, device="cuda", generator=gen) * 1e-2 for r, c in shapes]
+ws = m.muon_step_batched(W, G, M, m.MuonHparams(skip_nonfinite=True))
+m.adamw_step(W[0].view(-1), G[0].view(-1), M[0].view(-1), W[1].new_zeros(W[0].numel()), m.AdamwHparams(), 1)
+torch.cuda.synchronize()
+assert m.muon_query_status(ws) == 0
+torch.save([w.cpu() for w in W] + [x.cpu() for x in M], sys.argv[1])
+"""
+
+
+def test_debug_mode_synchronises_and_changes_nothing(lib, tmp_path):
+    """MUON_DEBUG=1 waits for every launch and names a failed one on stderr;
+    a clean run prints nothing and computes the same bits as a normal run
+    (each run in its own process: the variable is read once per process)."""
+    import os
+    import subprocess
+    import sys
+    from conftest import ROOT
+    script = tmp_path / "debug_step.py"
+    script.write_text(_DEBUG_SCRIPT)
+    out = {}
+    for flag in ("1", "0"):
+        path = tmp_path / f"out_{flag}.pt"
+        r = subprocess.run([sys.executable, str(script), str(path), ROOT], capture_output=True, text=True,
+                           env=dict(os.environ, MUON_DEBUG=flag), timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        assert "muon: kernel" not in r.stderr
+        out[flag] = torch.load(path)
+    for a, b in zip(out["1"], out["0"]):
+        assert torch.equal(a, b)
