@@ -157,7 +157,10 @@ muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count,
                                 size_t ws_bytes, void* stream);
 
 /* Per-matrix statistics of one step (no counterpart in the update itself;
- * the pages suggest watching such quantities, [OPT] section 5).  fp64:
+ * the closing notes of [OPT], after section 5.4, advise logging numerical
+ * statistics of the optimizer state to see trouble before the loss does;
+ * these are the Muon step's own: the norm it divides by and the RMS it
+ * matches).  fp64:
  *   u_norm      ||u||_F, the Frobenius norm of the look-ahead the step
  *               normalised: sqrt of the sum of the momentum pass's fp32
  *               tile sums of u^2, summed in fp64
