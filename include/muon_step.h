@@ -30,7 +30,7 @@ extern "C" {
 typedef enum {
     MUON_OK = 0,
     MUON_ERR_INVALID_ARG = 1,          /* null pointer, bad size, bad hparam  */
-    MUON_ERR_UNSUPPORTED_DTYPE = 2,    /* g_dtype not MUON_F32 / MUON_BF16    */
+    MUON_ERR_UNSUPPORTED_DTYPE = 2,    /* g_dtype not a muon_dtype_t          */
     MUON_ERR_MISALIGNED = 3,           /* pointer below its element alignment */
     MUON_ERR_WORKSPACE_TOO_SMALL = 4,  /* a single matrix needs more          */
     MUON_ERR_CUDA = 5,                 /* a CUDA runtime call failed          */
@@ -40,11 +40,14 @@ typedef enum {
                                           skipped the step; nothing changed   */
 } muon_status_t;
 
-typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype_t;
+/* Gradient element types.  Every one widens to fp32 exactly before the
+ * momentum update.  fp16 gradients are those of FP16 mixed-precision
+ * training, whose overflow to inf the guard of [OPT] section 5.4 catches. */
+typedef enum { MUON_F32 = 0, MUON_BF16 = 1, MUON_F16 = 2 } muon_dtype_t;
 
 /* One hidden weight matrix under Muon.  All three buffers are device memory
  * of rows*cols elements; W and M are fp32 and updated in place, G is read
- * only.  W, M and fp32 G must be 4-byte aligned, bf16 G 2-byte aligned;
+ * only.  W, M and fp32 G must be 4-byte aligned, bf16 or fp16 G 2-byte aligned;
  * 16-byte alignment enables the vectorised path.  Matrices of one call must
  * not overlap one another. */
 typedef struct {

@@ -31,7 +31,7 @@ LIB_PATH = os.path.join(_HERE, "libmuonstep.so")
 _lock = threading.Lock()
 _lib = None
 
-MUON_F32, MUON_BF16 = 0, 1
+MUON_F32, MUON_BF16, MUON_F16 = 0, 1, 2
 STATUS = {0: "MUON_OK", 1: "MUON_ERR_INVALID_ARG", 2: "MUON_ERR_UNSUPPORTED_DTYPE",
           3: "MUON_ERR_MISALIGNED", 4: "MUON_ERR_WORKSPACE_TOO_SMALL", 5: "MUON_ERR_CUDA",
           6: "MUON_ERR_TIMEOUT", 7: "MUON_ERR_NO_DEVICE", 8: "MUON_STEP_SKIPPED"}
@@ -258,6 +258,11 @@ def allocate_workspace(nbytes: int, device=None):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
 
 
+def _g_dtype(g) -> int:
+    import torch
+    return {torch.float32: MUON_F32, torch.bfloat16: MUON_BF16, torch.float16: MUON_F16}[g.dtype]
+
+
 def _stats_tensor(stats, n):
     import torch
     if not (isinstance(stats, torch.Tensor) and stats.is_cuda and stats.dtype == torch.float64
@@ -270,7 +275,7 @@ def muon_step_batched(W, G, M, hp: MuonHparams = MuonHparams(), workspace=None, 
                       budget_bytes: int = 16 << 30, stats=None):
     """One Muon step on lists of matrices (in place on every W and M).
 
-    W, M: fp32 CUDA tensors (rows x cols); G: fp32 or bf16 of the same shape.
+    W, M: fp32 CUDA tensors (rows x cols); G: fp32, bf16 or fp16 of the same shape.
     workspace: a uint8 CUDA tensor; allocated here (torch) when None.
     stats: optional CUDA float64 tensor (len(W), 2) that receives each
     matrix's (||u||_F, update RMS) (muon_step_batched_stats).
@@ -282,13 +287,13 @@ def muon_step_batched(W, G, M, hp: MuonHparams = MuonHparams(), workspace=None, 
     arr = (MuonMatrix * max(1, n))()
     for i in range(n):
         w = _dev_tensor(W[i], f"W[{i}]", (torch.float32,))
-        g = _dev_tensor(G[i], f"G[{i}]", (torch.float32, torch.bfloat16))
+        g = _dev_tensor(G[i], f"G[{i}]", (torch.float32, torch.bfloat16, torch.float16))
         m = _dev_tensor(M[i], f"M[{i}]", (torch.float32,))
         if w.dim() != 2 or w.shape != g.shape or w.shape != m.shape:
             raise ValueError(f"matrix {i}: W, G, M must be equal-shaped 2-D tensors")
         arr[i].W, arr[i].G, arr[i].M = w.data_ptr(), g.data_ptr(), m.data_ptr()
         arr[i].rows, arr[i].cols = w.shape
-        arr[i].g_dtype = MUON_BF16 if g.dtype == torch.bfloat16 else MUON_F32
+        arr[i].g_dtype = _g_dtype(g)
     lib = load_library()
     if workspace is None:
         need = ctypes.c_size_t(0)
@@ -320,13 +325,13 @@ def muon_step_batched_noalloc(W, G, M, hp: MuonHparams = MuonHparams(), stream=N
     arr = (MuonMatrix * max(1, n))()
     for i in range(n):
         w = _dev_tensor(W[i], f"W[{i}]", (torch.float32,))
-        g = _dev_tensor(G[i], f"G[{i}]", (torch.float32, torch.bfloat16))
+        g = _dev_tensor(G[i], f"G[{i}]", (torch.float32, torch.bfloat16, torch.float16))
         m = _dev_tensor(M[i], f"M[{i}]", (torch.float32,))
         if w.dim() != 2 or w.shape != g.shape or w.shape != m.shape:
             raise ValueError(f"matrix {i}: W, G, M must be equal-shaped 2-D tensors")
         arr[i].W, arr[i].G, arr[i].M = w.data_ptr(), g.data_ptr(), m.data_ptr()
         arr[i].rows, arr[i].cols = w.shape
-        arr[i].g_dtype = MUON_BF16 if g.dtype == torch.bfloat16 else MUON_F32
+        arr[i].g_dtype = _g_dtype(g)
     h = hp._c()
     _check(load_library().muon_step_batched_noalloc(ctypes.cast(arr, ctypes.c_void_p), n,
                                                     ctypes.byref(h), _stream(stream)),
@@ -430,13 +435,13 @@ class MuonBatch:
         self.arr = (MuonMatrix * max(1, n))()
         for i in range(n):
             w = _dev_tensor(W[i], f"W[{i}]", (torch.float32,))
-            g = _dev_tensor(G[i], f"G[{i}]", (torch.float32, torch.bfloat16))
+            g = _dev_tensor(G[i], f"G[{i}]", (torch.float32, torch.bfloat16, torch.float16))
             m = _dev_tensor(M[i], f"M[{i}]", (torch.float32,))
             if w.dim() != 2 or w.shape != g.shape or w.shape != m.shape:
                 raise ValueError(f"matrix {i}: W, G, M must be equal-shaped 2-D tensors")
             self.arr[i].W, self.arr[i].G, self.arr[i].M = w.data_ptr(), g.data_ptr(), m.data_ptr()
             self.arr[i].rows, self.arr[i].cols = w.shape
-            self.arr[i].g_dtype = MUON_BF16 if g.dtype == torch.bfloat16 else MUON_F32
+            self.arr[i].g_dtype = _g_dtype(g)
         lib = load_library()
         if workspace is None:
             need = ctypes.c_size_t(0)

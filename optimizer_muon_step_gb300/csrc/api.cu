@@ -122,8 +122,9 @@ muon_status_t check_pointers(const muon_matrix_t* mats, int64_t count) {
     for (int64_t i = 0; i < count; ++i) {
         const muon_matrix_t& m = mats[i];
         if (!m.W || !m.G || !m.M || m.reserved != 0) return MUON_ERR_INVALID_ARG;
-        if (m.g_dtype != MUON_F32 && m.g_dtype != MUON_BF16) return MUON_ERR_UNSUPPORTED_DTYPE;
-        const uintptr_t g_align = m.g_dtype == MUON_BF16 ? 2 : 4;
+        if (m.g_dtype != MUON_F32 && m.g_dtype != MUON_BF16 && m.g_dtype != MUON_F16)
+            return MUON_ERR_UNSUPPORTED_DTYPE;
+        const uintptr_t g_align = m.g_dtype == MUON_F32 ? 4 : 2;
         if ((reinterpret_cast<uintptr_t>(m.W) & 3u) || (reinterpret_cast<uintptr_t>(m.M) & 3u) ||
             (reinterpret_cast<uintptr_t>(m.G) & (g_align - 1)))
             return MUON_ERR_MISALIGNED;
@@ -331,7 +332,8 @@ muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hpa
     int max_wide_tiles = 0;  // flat tiles of the wide matrices (momentum pass)
     int max_units = 0;       // tall-pass units (momentum pass)
     int64_t max_final_units = 0;  // tall units of the final update
-    int tall_units[2] = {0, 0};  // the same, over tall matrices with fp32 / bf16 gradients
+    int tall_units[3] = {0, 0, 0};  // the same, over tall matrices per gradient type (muon_dtype_t)
+    int wide_tiles[3] = {0, 0, 0};  // flat tiles of the wide matrices per gradient type
     float* o_partials = nullptr;  // statistics pass: kStatsTiles sums per matrix after the norm partials
 
     // Fills `descs` and the layout for plan rows [b, e) and uploads them (by
@@ -347,7 +349,8 @@ muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hpa
         max_tiles = 1;
         max_wide_tiles = max_units = 0;
         max_final_units = 0;
-        tall_units[0] = tall_units[1] = 0;
+        tall_units[0] = tall_units[1] = tall_units[2] = 0;
+        wide_tiles[0] = wide_tiles[1] = wide_tiles[2] = 0;
         for (int k = 0; k < n; ++k) {
             const PlanRow& row = plan[b + k];
             const muon_matrix_t& m = mats[row.idx];
@@ -370,7 +373,7 @@ muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hpa
             }
             d.tile_len = tl;
             d.ntiles = static_cast<int32_t>(nt);
-            d.g_bf16 = m.g_dtype == MUON_BF16 ? 1 : 0;
+            d.g_kind = m.g_dtype;
             d.transposed = row.transposed;
             d.vec = ((reinterpret_cast<uintptr_t>(m.W) | reinterpret_cast<uintptr_t>(m.G) |
                       reinterpret_cast<uintptr_t>(m.M)) & 15u) == 0 ? 1 : 0;
@@ -388,10 +391,11 @@ muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hpa
                 d.nparts = static_cast<int32_t>(cu * ((rt + kr - 1) / kr));
                 max_units = std::max(max_units, d.nparts);
                 max_final_units = std::max(max_final_units, final_update_tall_units(m.rows, m.cols));
-                tall_units[d.g_bf16] = std::max(tall_units[d.g_bf16], d.nparts);
+                tall_units[d.g_kind] = std::max(tall_units[d.g_kind], d.nparts);
             } else {
                 d.nparts = d.ntiles;
                 max_wide_tiles = std::max(max_wide_tiles, d.ntiles);
+                wide_tiles[d.g_kind] = std::max(wide_tiles[d.g_kind], d.ntiles);
             }
             max_tiles = std::max(max_tiles, d.ntiles);
         }
@@ -436,7 +440,7 @@ muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hpa
             s = prepare_chunk(b, e);
             if (s != MUON_OK) return s;
         }
-        s = from_cuda(launch_momentum_norm(d_descs, n, max_wide_tiles, tall_units[1], tall_units[0], ms, st));
+        s = from_cuda(launch_momentum_norm(d_descs, n, wide_tiles, tall_units, ms, st));
         if (s != MUON_OK) return s;
         // with no NS step X0 is the result, so it is normalised in place
         s = from_cuda(launch_norm_finalize(d_descs, n, hp->norm_eps, hp->ns_steps == 0 ? 1 : 0, st));

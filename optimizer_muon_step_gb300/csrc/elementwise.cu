@@ -22,6 +22,7 @@
 // __fadd_rn, ...) so no multiply-add is contracted and the results are
 // reproducible bit for bit.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <string.h>
 
 #include <memory>
@@ -43,9 +44,28 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-__device__ __forceinline__ float load_g(const void* G, int g_bf16, int64_t i) {
-    return g_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(G)[i])
-                  : static_cast<const float*>(G)[i];
+// A 2-byte gradient element as fp32 (exact): bf16 or fp16 bits.
+__device__ __forceinline__ float half_g_to_f32(uint32_t h, int g_kind) {
+    return g_kind == MUON_F16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
+                              : __uint_as_float(h << 16);
+}
+
+// Two packed 2-byte gradient elements (the lower-addressed one in the low
+// half) as fp32.
+__device__ __forceinline__ void unpack_g2(uint32_t w, int g_kind, float& lo, float& hi) {
+    if (g_kind == MUON_F16) {
+        lo = __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+        hi = __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+    } else {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xffff0000u);
+    }
+}
+
+// Element i of a gradient of type g_kind (muon_dtype_t) as fp32.
+__device__ __forceinline__ float load_g(const void* G, int g_kind, int64_t i) {
+    return g_kind == MUON_F32 ? static_cast<const float*>(G)[i]
+                              : half_g_to_f32(static_cast<const uint16_t*>(G)[i], g_kind);
 }
 
 // The gradient as the momentum sees it: clip * G when global-norm clipping
@@ -82,12 +102,16 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // X0 = bf16(u) and a per-tile sum of squares.
 // grid = (max tiles, matrices); each CTA handles one contiguous tile.
 // ---------------------------------------------------------------------------
+// One instance per gradient type (KIND, a muon_dtype_t), whose conversion
+// it compiles in.
+template <int KIND>
 __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* __restrict__ descs,
                                                                  MomentumScalars s) {
     __shared__ float red[kThreads / 32];
     const MatDesc& d = descs[blockIdx.y];
     const int tile = blockIdx.x;
-    if (d.transposed || tile >= d.ntiles) return;  // tall matrices: momentum_tall_kernel
+    // tall matrices: momentum_tall_kernel; other gradient types: their instance
+    if (d.transposed || tile >= d.ntiles || d.g_kind != KIND) return;
     if (s.header && s.header->skip) return;  // the non-finite guard skips the step
     const float clip = s.scale_g ? s.header->clip : 1.f;
     const int64_t n = d.rows * d.cols;
@@ -95,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
     const int64_t end = min(n, start + d.tile_len);
     float* __restrict__ M = d.M;
     const void* G = d.G;
-    const int g_bf16 = d.g_bf16;
+    constexpr int g_kind = KIND;
     uint16_t* __restrict__ X0 = d.X0;
     const int64_t cols = d.cols, ldx = d.ldx;
     const bool x_flat = ldx == cols;  // X0 rows packed: X0 index = element index
@@ -106,14 +130,11 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
         for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
             const int64_t i = start + (v << 3);
             float g[8];
-            if (g_bf16) {
+            if constexpr (KIND != MUON_F32) {
                 uint4 raw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(G) + i));
                 const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    g[2 * j] = __uint_as_float(w[j] << 16);
-                    g[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-                }
+                for (int j = 0; j < 4; ++j) unpack_g2(w[j], KIND, g[2 * j], g[2 * j + 1]);
             } else {
                 const float4* gp = reinterpret_cast<const float4*>(static_cast<const float*>(G) + i);
                 float4 a = __ldg(gp), b = __ldg(gp + 1);
@@ -144,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
     }
     for (int64_t i = scalar_from + threadIdx.x; i < end; i += kThreads) {
         float m = M[i];
-        float u = momentum_elem(scaled_g(load_g(G, g_bf16, i), s.scale_g, clip), m, s);
+        float u = momentum_elem(scaled_g(load_g(G, g_kind, i), s.scale_g, clip), m, s);
         M[i] = m;
         acc = fmaf(u, u, acc);
         X0[(i / cols) * ldx + i % cols] = f32_to_bf16(u);
@@ -160,7 +181,7 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
 // one partial.  grid = (max units, matrices).
 // Thread (tx, ty) covers rows ty + 16 i (i < 4) and columns 4 tx .. 4 tx + 3.
 // ---------------------------------------------------------------------------
-// kPrefetch (bf16 gradients): the next full tile's G and M are loaded into
+// kPrefetch (2-byte gradients, bf16 or fp16): the next full tile's G and M are loaded into
 // registers right after the current tile's momentum step, so they are in
 // flight during its barriers and transposed X0 stores; four CTAs fit an SM
 // (at most 64 registers a thread).  Without it (fp32 gradients, whose tiles
@@ -168,15 +189,17 @@ __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* 
 // Measured: prefetching made the bf16 pass 6% faster and the fp32 one 8%
 // slower; at the unbounded 118 registers only two CTAs fit and the kernel
 // ran at a third of HBM bandwidth.  Each instance handles the tall matrices
-// of its gradient type.
-template <bool kPrefetch>
-__global__ void __launch_bounds__(kThreads, kPrefetch ? 4 : 6) momentum_tall_kernel(const MatDesc* __restrict__ descs,
-                                                                                  MomentumScalars s) {
+// of one gradient type (KIND, a muon_dtype_t), whose conversion it compiles
+// in.
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, KIND != MUON_F32 ? 4 : 6) momentum_tall_kernel(
+    const MatDesc* __restrict__ descs, MomentumScalars s) {
+    constexpr bool kPrefetch = KIND != MUON_F32;
     __shared__ uint16_t tileT[kTile][kTile + 2];
     __shared__ float red[kThreads / 32];
     const MatDesc& d = descs[blockIdx.y];
     const int unit = blockIdx.x;
-    if (!d.transposed || unit >= d.nparts || (d.g_bf16 != 0) != kPrefetch) return;
+    if (!d.transposed || unit >= d.nparts || d.g_kind != KIND) return;
     if (s.header && s.header->skip) return;
     const float clip = s.scale_g ? s.header->clip : 1.f;
     const int64_t rows = d.rows, cols = d.cols;
@@ -189,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, kPrefetch ? 4 : 6) momentum_tall_ker
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     float* __restrict__ M = d.M;
     const void* G = d.G;
-    const int g_bf16 = d.g_bf16;
+    constexpr int g_kind = KIND;
     uint16_t* __restrict__ X0 = d.X0;
     const int64_t ldx = d.ldx;
     const int64_t nr = rt_end - rt_begin;
@@ -206,12 +229,10 @@ __global__ void __launch_bounds__(kThreads, kPrefetch ? 4 : 6) momentum_tall_ker
     auto load_row = [&](int i, int64_t r0, int64_t c0, float4& m4, float (&g)[4]) {
         const int64_t off = (r0 + ty + 16 * i) * cols + c0 + 4 * tx;
         m4 = *reinterpret_cast<const float4*>(M + off);
-        if (g_bf16) {
+        if constexpr (KIND != MUON_F32) {
             const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(G) + off));
-            g[0] = __uint_as_float(raw.x << 16);
-            g[1] = __uint_as_float(raw.x & 0xffff0000u);
-            g[2] = __uint_as_float(raw.y << 16);
-            g[3] = __uint_as_float(raw.y & 0xffff0000u);
+            unpack_g2(raw.x, KIND, g[0], g[1]);
+            unpack_g2(raw.y, KIND, g[2], g[3]);
         } else {
             const float4 g4 = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(G) + off));
             g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
@@ -261,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, kPrefetch ? 4 : 6) momentum_tall_ker
                     if (r < rows && c + j < cols) {
                         const int64_t off = r * cols + c + j;
                         float m = M[off];
-                        const float u = momentum_elem(scaled_g(load_g(G, g_bf16, off), s.scale_g, clip), m, s);
+                        const float u = momentum_elem(scaled_g(load_g(G, g_kind, off), s.scale_g, clip), m, s);
                         M[off] = m;
                         acc = fmaf(u, u, acc);
                         b[j] = f32_to_bf16(u);
@@ -546,7 +567,7 @@ __global__ void __launch_bounds__(kThreads) grad_stats_kernel(const MatDesc* __r
     const int64_t start = static_cast<int64_t>(tile) * d.tile_len;
     const int64_t end = min(n, static_cast<int64_t>(last) * d.tile_len);
     const void* G = d.G;
-    const int g_bf16 = d.g_bf16;
+    const int g_kind = d.g_kind;
     float acc = 0.f;
     unsigned int bad = 0;
     int64_t scalar_from = start;
@@ -555,13 +576,15 @@ __global__ void __launch_bounds__(kThreads) grad_stats_kernel(const MatDesc* __r
         for (int64_t v = threadIdx.x; v < nvec; v += kThreads) {
             const int64_t i = start + (v << 3);
             float g[8];
-            if (g_bf16) {
+            if (g_kind != MUON_F32) {
                 uint4 raw = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(G) + i));
                 const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                if (g_kind == MUON_F16) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    g[2 * j] = __uint_as_float(w[j] << 16);
-                    g[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+                    for (int j = 0; j < 4; ++j) unpack_g2(w[j], MUON_F16, g[2 * j], g[2 * j + 1]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) unpack_g2(w[j], MUON_BF16, g[2 * j], g[2 * j + 1]);
                 }
             } else {
                 const float4* gp = reinterpret_cast<const float4*>(static_cast<const float*>(G) + i);
@@ -578,7 +601,7 @@ __global__ void __launch_bounds__(kThreads) grad_stats_kernel(const MatDesc* __r
         scalar_from = start + (nvec << 3);
     }
     for (int64_t i = scalar_from + threadIdx.x; i < end; i += kThreads) {
-        const float g = load_g(G, g_bf16, i);
+        const float g = load_g(G, g_kind, i);
         acc = fmaf(g, g, acc);
         bad += isfinite(g) ? 0u : 1u;
     }
@@ -733,26 +756,41 @@ cudaError_t launch_desc_upload(MatDesc* d_descs, const MatDesc* descs, int count
     return cudaSuccess;
 }
 
-// max_tiles: largest ntiles over the wide matrices; tall_bf16 / tall_f32:
-// largest nparts over the tall matrices with bf16 / fp32 gradients (0 when
-// there are none of that kind).
-cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles, int tall_bf16, int tall_f32,
+// wide_tiles[k]: largest ntiles over the wide matrices, tall_units[k]:
+// largest nparts over the tall matrices, whose gradient type is k (a
+// muon_dtype_t; 0 when there are none of that type).
+cudaError_t launch_momentum_norm(const MatDesc* descs, int count, const int* wide_tiles, const int* tall_units,
                                  MomentumScalars s, cudaStream_t st) {
     for (int off = 0; off < count; off += 65535) {
         int n = count - off < 65535 ? count - off : 65535;
-        if (max_tiles > 0) {
+        if (wide_tiles[MUON_BF16] > 0) {
             launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-            momentum_norm_kernel<<<dim3(max_tiles, n), kThreads, 0, st>>>(descs + off, s);
+            momentum_norm_kernel<MUON_BF16><<<dim3(wide_tiles[MUON_BF16], n), kThreads, 0, st>>>(descs + off, s);
             launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
         }
-        if (tall_bf16 > 0) {
+        if (wide_tiles[MUON_F16] > 0) {
             launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-            momentum_tall_kernel<true><<<dim3(tall_bf16, n), kThreads, 0, st>>>(descs + off, s);
+            momentum_norm_kernel<MUON_F16><<<dim3(wide_tiles[MUON_F16], n), kThreads, 0, st>>>(descs + off, s);
             launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
         }
-        if (tall_f32 > 0) {
+        if (wide_tiles[MUON_F32] > 0) {
             launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-            momentum_tall_kernel<false><<<dim3(tall_f32, n), kThreads, 0, st>>>(descs + off, s);
+            momentum_norm_kernel<MUON_F32><<<dim3(wide_tiles[MUON_F32], n), kThreads, 0, st>>>(descs + off, s);
+            launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
+        }
+        if (tall_units[MUON_BF16] > 0) {
+            launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
+            momentum_tall_kernel<MUON_BF16><<<dim3(tall_units[MUON_BF16], n), kThreads, 0, st>>>(descs + off, s);
+            launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
+        }
+        if (tall_units[MUON_F16] > 0) {
+            launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
+            momentum_tall_kernel<MUON_F16><<<dim3(tall_units[MUON_F16], n), kThreads, 0, st>>>(descs + off, s);
+            launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
+        }
+        if (tall_units[MUON_F32] > 0) {
+            launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
+            momentum_tall_kernel<MUON_F32><<<dim3(tall_units[MUON_F32], n), kThreads, 0, st>>>(descs + off, s);
             launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
         }
     }

@@ -24,7 +24,7 @@ struct MatDesc {
     int64_t ldx;         // row stride of X0 / O in elements
     int64_t tile_len;    // elements per flat tile (multiple of 8): wide momentum pass, gradient guard
     int32_t ntiles;      // flat tiles
-    int32_t g_bf16;      // 1: G is bf16
+    int32_t g_kind;      // G's element type: 0 fp32, 1 bf16, 2 fp16 (muon_dtype_t)
     int32_t transposed;  // 1: rows > cols, X holds the transpose
     int32_t vec;         // 1: W, G, M are 16-byte aligned
     float scale;         // 1 / (||u||_F + eps), written by the finalize kernel
@@ -108,9 +108,10 @@ cudaError_t launch_desc_upload(MatDesc* d_descs, const MatDesc* descs, int count
 // ---- element-wise kernels (elementwise.cu) --------------------------------
 // Momentum pass: M updated, X0 = bf16(u) in the wide orientation (tall
 // matrices through a tiled transpose), per-unit sums of u^2 into the
-// partials.  `tall_bf16` / `tall_f32` bound nparts over the tall matrices
-// with bf16 / fp32 gradients.
-cudaError_t launch_momentum_norm(const MatDesc* descs, int count, int max_tiles, int tall_bf16, int tall_f32,
+// partials.  wide_tiles[k] bounds ntiles over the wide matrices and
+// tall_units[k] nparts over the tall ones whose gradient type is k (3
+// entries each, one per muon_dtype_t).
+cudaError_t launch_momentum_norm(const MatDesc* descs, int count, const int* wide_tiles, const int* tall_units,
                                  MomentumScalars s, cudaStream_t st);
 // Norm: scale = 1 / (||u|| + eps) per matrix; the first NS step applies
 // ns_scale to X0 = bf16(u).  Normally ns_scale = scale.  A norm outside the
