@@ -280,6 +280,30 @@ muon_status_t adamw_step(float* p, const float* g, float* m, float* v,
                          int64_t n, const adamw_hparams_t* hp, int64_t step,
                          void* stream);
 
+/* One tensor of a multi-tensor AdamW step: n fp32 elements in each of four
+ * device buffers (any shape, contiguous), p, m, v updated in place. */
+typedef struct {
+    float* p;
+    const float* g;
+    float* m;
+    float* v;
+    int64_t n;
+} adamw_tensor_t;
+
+/* AdamW on `count` tensors (host array) with one set of hyper-parameters
+ * and one step count: every tensor is updated exactly as adamw_step would
+ * update it, bit for bit, in one launch per 448 tensors.  The rest of the
+ * parameters besides Muon's matrices -- embedding, LM head, norm gains and
+ * biases ([OPT] section 4.3) -- are many tensors, most of them small.
+ *   - each tensor follows adamw_step's rules (4-byte aligned buffers, its
+ *     four buffers disjoint); 16-byte alignment of all four enables the
+ *     vector path for that tensor;
+ *   - no buffer of one tensor may overlap a buffer of another;
+ *   - n == 0 tensors are skipped; count == 0 is a no-op.
+ * Errors as adamw_step's; nothing is enqueued when one tensor fails a check. */
+muon_status_t adamw_step_batched(const adamw_tensor_t* tensors, int64_t count,
+                                 const adamw_hparams_t* hp, int64_t step, void* stream);
+
 /* Failure-detection self-check (no counterpart on the pages).  Enqueues on
  * `stream` one thread that waits, through the same bounded mbarrier wait as
  * the Newton-Schulz kernels, on a barrier nothing ever arrives on.  After

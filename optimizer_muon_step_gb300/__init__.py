@@ -10,6 +10,7 @@ Functions keep the C names:
     muon_step_batched(W, G, M, hp, workspace=None, stream=None)
     muon_newton_schulz(X, steps, coeffs, out=None, workspace=None, stream=None)
     adamw_step(p, g, m, v, hp, step, stream=None)
+    adamw_step_batched([(p, g, m, v), ...], hp, step, stream=None)
     muon_plan(shapes, ws_bytes)
     muon_workspace_bytes_per_matrix(rows, cols)
     muon_workspace_size(shapes, budget_bytes)
@@ -43,7 +44,7 @@ EXPORTS = ("muon_workspace_bytes_per_matrix", "muon_workspace_size", "muon_plan"
            "muon_status_string", "muon_version", "muon_launch_count", "muon_set_timing",
            "muon_timing_read", "muon_kernel_name", "muon_step_batched_noalloc",
            "muon_check_bounded_wait", "muon_step_graph_create", "muon_step_graph_launch",
-           "muon_step_graph_destroy", "muon_step_batched_stats")
+           "muon_step_graph_destroy", "muon_step_batched_stats", "adamw_step_batched")
 KERNEL_KINDS = ("momentum_norm", "norm_finalize", "x0_rescale", "ns_syrk", "ns_poly",
                 "ns_update", "final_update", "adamw", "grad_guard", "desc_upload", "stats")
 
@@ -165,6 +166,8 @@ def load_library(path: str = LIB_PATH):
         lib.muon_newton_schulz.argtypes = [P, P, i64, i64, i64, i32, P, i32, P, ctypes.c_size_t, P]
         lib.muon_newton_schulz.restype = ctypes.c_int
         lib.adamw_step.argtypes = [P, P, P, P, i64, P, i64, P]
+        lib.adamw_step_batched.argtypes = [P, i64, P, i64, P]
+        lib.adamw_step_batched.restype = ctypes.c_int
         lib.adamw_step.restype = ctypes.c_int
         lib.muon_query_status.argtypes = [P, P]
         lib.muon_query_status.restype = ctypes.c_int
@@ -377,6 +380,31 @@ def adamw_step(p, g, m, v, hp: AdamwHparams = AdamwHparams(), step: int = 1, str
     _check(load_library().adamw_step(ctypes.c_void_p(p.data_ptr()), ctypes.c_void_p(g.data_ptr()),
                                      ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()),
                                      n, ctypes.byref(h), int(step), _stream(stream)), "adamw_step")
+
+
+class AdamwTensor(ctypes.Structure):
+    _fields_ = [("p", ctypes.c_void_p), ("g", ctypes.c_void_p), ("m", ctypes.c_void_p),
+                ("v", ctypes.c_void_p), ("n", ctypes.c_int64)]
+
+
+def adamw_step_batched(tensors, hp: AdamwHparams = AdamwHparams(), step: int = 1, stream=None):
+    """AdamW in place on many tensors in few launches: `tensors` is a list of
+    (p, g, m, v) contiguous fp32 CUDA tensors, the four of a tuple with equal
+    element counts (any shapes)."""
+    import torch
+    arr = (AdamwTensor * max(1, len(tensors)))()
+    for i, quad in enumerate(tensors):
+        p, g, m, v = quad
+        for name, x in (("p", p), ("g", g), ("m", m), ("v", v)):
+            _dev_tensor(x, f"{name}[{i}]", (torch.float32,))
+        n = p.numel()
+        if not (g.numel() == m.numel() == v.numel() == n):
+            raise ValueError(f"tensor {i}: p, g, m, v must have the same number of elements")
+        arr[i].p, arr[i].g, arr[i].m, arr[i].v = p.data_ptr(), g.data_ptr(), m.data_ptr(), v.data_ptr()
+        arr[i].n = n
+    h = hp._c()
+    _check(load_library().adamw_step_batched(ctypes.cast(arr, ctypes.c_void_p), len(tensors), ctypes.byref(h),
+                                             int(step), _stream(stream)), "adamw_step_batched")
 
 
 def muon_query_status(workspace, stream=None) -> int:

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmuonstep.so")
-SOURCES = ["api.cu", "elementwise.cu", "ns_gemm.cu", "timing.cu", "noalloc.cu", "stats.cu"]
+SOURCES = ["api.cu", "elementwise.cu", "ns_gemm.cu", "timing.cu", "noalloc.cu", "stats.cu", "adamw_multi.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -611,42 +611,101 @@ muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t 
     return MUON_OK;
 }
 
-muon_status_t adamw_step(float* p, const float* g, float* m, float* v, int64_t n, const adamw_hparams_t* hp,
-                         int64_t step, void* stream) {
-    NvtxScope range("adamw_step");
-    if (!hp || n < 0 || step < 1) return MUON_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// AdamW hyper-parameters and step count -> the kernels' scalars, with the
+// bias corrections 1 - beta^step computed in fp64 and rounded to fp32.
+muon_status_t adamw_scalars(const adamw_hparams_t* hp, int64_t step, AdamwScalars* sc) {
+    if (!hp || step < 1) return MUON_ERR_INVALID_ARG;
     if (!finite(hp->lr) || !finite(hp->beta1) || !finite(hp->beta2) || !finite(hp->eps) ||
         !finite(hp->weight_decay))
         return MUON_ERR_INVALID_ARG;
     if (hp->beta1 < 0.f || hp->beta1 >= 1.f || hp->beta2 < 0.f || hp->beta2 >= 1.f || hp->eps < 0.f)
         return MUON_ERR_INVALID_ARG;
-    if (n == 0) return MUON_OK;
+    sc->lr = hp->lr;
+    sc->beta1 = hp->beta1;
+    sc->beta2 = hp->beta2;
+    sc->one_minus_beta1 = 1.0f - hp->beta1;
+    sc->one_minus_beta2 = 1.0f - hp->beta2;
+    sc->bc1 = static_cast<float>(1.0 - pow(static_cast<double>(hp->beta1), static_cast<double>(step)));
+    sc->bc2 = static_cast<float>(1.0 - pow(static_cast<double>(hp->beta2), static_cast<double>(step)));
+    sc->eps = hp->eps;
+    sc->weight_decay = hp->weight_decay;
+    if (!(sc->bc1 > 0.f) || !(sc->bc2 > 0.f)) return MUON_ERR_INVALID_ARG;
+    return MUON_OK;
+}
+
+// One AdamW tensor's pointer checks: non-null, 4-byte aligned.
+muon_status_t check_adamw_tensor(const float* p, const float* g, const float* m, const float* v) {
     if (!p || !g || !m || !v) return MUON_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(m) |
          reinterpret_cast<uintptr_t>(v)) & 3u)
         return MUON_ERR_MISALIGNED;
-    // the four buffers must be pairwise disjoint
-    const uintptr_t lo[4] = {reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(g),
-                             reinterpret_cast<uintptr_t>(m), reinterpret_cast<uintptr_t>(v)};
-    const uintptr_t len = static_cast<uintptr_t>(n) * 4u;
-    for (int i = 0; i < 4; ++i)
-        for (int j = i + 1; j < 4; ++j)
-            if (lo[i] < lo[j] + len && lo[j] < lo[i] + len) return MUON_ERR_INVALID_ARG;
-    int num_sms = 0;
-    muon_status_t s = device_info(&num_sms);
-    if (s != MUON_OK) return s;
+    return MUON_OK;
+}
+
+// Whether byte ranges [start, end) are pairwise disjoint (sorted in place).
+bool disjoint(std::vector<std::pair<uintptr_t, uintptr_t>>& ranges) {
+    std::sort(ranges.begin(), ranges.end());
+    for (size_t i = 1; i < ranges.size(); ++i)
+        if (ranges[i].first < ranges[i - 1].second) return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+muon_status_t adamw_step(float* p, const float* g, float* m, float* v, int64_t n, const adamw_hparams_t* hp,
+                         int64_t step, void* stream) {
+    NvtxScope range("adamw_step");
     AdamwScalars sc;
-    sc.lr = hp->lr;
-    sc.beta1 = hp->beta1;
-    sc.beta2 = hp->beta2;
-    sc.one_minus_beta1 = 1.0f - hp->beta1;
-    sc.one_minus_beta2 = 1.0f - hp->beta2;
-    sc.bc1 = static_cast<float>(1.0 - pow(static_cast<double>(hp->beta1), static_cast<double>(step)));
-    sc.bc2 = static_cast<float>(1.0 - pow(static_cast<double>(hp->beta2), static_cast<double>(step)));
-    sc.eps = hp->eps;
-    sc.weight_decay = hp->weight_decay;
-    if (!(sc.bc1 > 0.f) || !(sc.bc2 > 0.f)) return MUON_ERR_INVALID_ARG;
+    muon_status_t s = adamw_scalars(hp, step, &sc);
+    if (s != MUON_OK) return s;
+    if (n < 0) return MUON_ERR_INVALID_ARG;
+    if (n == 0) return MUON_OK;
+    s = check_adamw_tensor(p, g, m, v);
+    if (s != MUON_OK) return s;
+    // the four buffers must be pairwise disjoint
+    const uintptr_t len = static_cast<uintptr_t>(n) * 4u;
+    std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
+    for (const void* b : {static_cast<const void*>(p), static_cast<const void*>(g), static_cast<const void*>(m),
+                          static_cast<const void*>(v)})
+        ranges.emplace_back(reinterpret_cast<uintptr_t>(b), reinterpret_cast<uintptr_t>(b) + len);
+    if (!disjoint(ranges)) return MUON_ERR_INVALID_ARG;
+    int num_sms = 0;
+    s = device_info(&num_sms);
+    if (s != MUON_OK) return s;
     return from_cuda(launch_adamw(p, g, m, v, n, sc, num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+muon_status_t adamw_step_batched(const adamw_tensor_t* tensors, int64_t count, const adamw_hparams_t* hp,
+                                 int64_t step, void* stream) {
+    NvtxScope range("adamw_step_batched");
+    AdamwScalars sc;
+    muon_status_t s = adamw_scalars(hp, step, &sc);
+    if (s != MUON_OK) return s;
+    if (count < 0 || (count > 0 && !tensors)) return MUON_ERR_INVALID_ARG;
+    std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
+    for (int64_t i = 0; i < count; ++i) {
+        const adamw_tensor_t& x = tensors[i];
+        if (x.n < 0 || x.n > (int64_t(1) << 40)) return MUON_ERR_INVALID_ARG;
+        if (x.n == 0) continue;
+        s = check_adamw_tensor(x.p, x.g, x.m, x.v);
+        if (s != MUON_OK) return s;
+        const uintptr_t len = static_cast<uintptr_t>(x.n) * 4u;
+        for (const void* b : {static_cast<const void*>(x.p), static_cast<const void*>(x.g),
+                              static_cast<const void*>(x.m), static_cast<const void*>(x.v)})
+            ranges.emplace_back(reinterpret_cast<uintptr_t>(b), reinterpret_cast<uintptr_t>(b) + len);
+    }
+    if (ranges.empty()) return MUON_OK;
+    if (!disjoint(ranges)) return MUON_ERR_INVALID_ARG;
+    int num_sms = 0;
+    s = device_info(&num_sms);
+    if (s != MUON_OK) return s;
+    return from_cuda(launch_adamw_multi(tensors, count, sc, num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 muon_status_t muon_check_bounded_wait(void* workspace, int64_t limit_us, void* stream) {

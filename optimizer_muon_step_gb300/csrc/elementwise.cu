@@ -656,20 +656,6 @@ __global__ void grad_decide_kernel(WsHeader* __restrict__ header, float max_grad
 // ---------------------------------------------------------------------------
 // AdamW
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void adamw_elem(float& p, float g, float& m, float& v, const AdamwScalars& s) {
-    float mi = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.one_minus_beta1, g));
-    float g2 = __fmul_rn(g, g);
-    float vi = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(s.one_minus_beta2, g2));
-    float m_hat = __fdiv_rn(mi, s.bc1);
-    float v_hat = __fdiv_rn(vi, s.bc2);
-    float den = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
-    float upd = __fdiv_rn(m_hat, den);
-    float decay = __fmul_rn(s.weight_decay, p);
-    p = __fsub_rn(p, __fmul_rn(s.lr, __fadd_rn(upd, decay)));
-    m = mi;
-    v = vi;
-}
-
 __global__ void __launch_bounds__(kThreads) adamw_vec_kernel(float4* __restrict__ p, const float4* __restrict__ g,
                                                              float4* __restrict__ m, float4* __restrict__ v,
                                                              int64_t nvec, AdamwScalars s) {

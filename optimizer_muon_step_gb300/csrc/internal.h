@@ -76,6 +76,26 @@ struct AdamwScalars {
     float bc1, bc2, eps, weight_decay;
 };
 
+#ifdef __CUDACC__
+// One AdamW element ("LLM training series, part 2: optimizers", sections 2.3
+// and 3.1), each operation a separately rounded fp32 op in this order:
+//   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g g
+//   p = p - lr ((m / bc1) / (sqrt(v / bc2) + eps) + wd p)
+__device__ __forceinline__ void adamw_elem(float& p, float g, float& m, float& v, const AdamwScalars& s) {
+    const float mi = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.one_minus_beta1, g));
+    const float g2 = __fmul_rn(g, g);
+    const float vi = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(s.one_minus_beta2, g2));
+    const float m_hat = __fdiv_rn(mi, s.bc1);
+    const float v_hat = __fdiv_rn(vi, s.bc2);
+    const float den = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
+    const float upd = __fdiv_rn(m_hat, den);
+    const float decay = __fmul_rn(s.weight_decay, p);
+    p = __fsub_rn(p, __fmul_rn(s.lr, __fadd_rn(upd, decay)));
+    m = mi;
+    v = vi;
+}
+#endif
+
 // ---- launch accounting (timing.cu) -----------------------------------------
 // Every kernel launch is bracketed by launch_begin / launch_end: they count
 // launches, open and close an NVTX range named for the kernel kind, and,
@@ -129,6 +149,10 @@ cudaError_t launch_final_update(const MatDesc* descs, int count, int max_wide_ti
                                 UpdateScalars s, cudaStream_t st);
 cudaError_t launch_adamw(float* p, const float* g, float* m, float* v, int64_t n,
                          AdamwScalars s, int num_sms, cudaStream_t st);
+// Multi-tensor AdamW (adamw_multi.cu): every tensor of the host array updated
+// exactly as launch_adamw would, one launch per 448 tensors.
+cudaError_t launch_adamw_multi(const adamw_tensor_t* tensors, int64_t count, AdamwScalars s, int num_sms,
+                               cudaStream_t st);
 // Gradient guard: per-tile sums of G^2 into the partials and a count of
 // non-finite elements into the header; then, per chunk, the partials summed
 // in order into header->sumsq; finally the clip factor and skip flag.

@@ -212,6 +212,31 @@ def test_stats_argument_validation(built):
     assert lib.muon_step_batched_stats(None, 0, ctypes.byref(_hp()), None, 0, P(8192), None) == 0
 
 
+def test_adamw_batched_argument_validation(built):
+    lib = built
+    P = ctypes.c_void_p
+    h = m.AdamwHparams()._c()
+    arr = (m.AdamwTensor * 2)()
+    for i, base in enumerate((1 << 20, 1 << 24)):
+        arr[i].p, arr[i].g, arr[i].m, arr[i].v = base, base + 4096, base + 8192, base + 12288
+        arr[i].n = 256
+    assert lib.adamw_step_batched(None, 2, ctypes.byref(h), 1, None) == 1        # no table
+    assert lib.adamw_step_batched(arr, 2, None, 1, None) == 1                     # no hparams
+    assert lib.adamw_step_batched(arr, 2, ctypes.byref(h), 0, None) == 1          # step < 1
+    assert lib.adamw_step_batched(arr, -1, ctypes.byref(h), 1, None) == 1
+    assert lib.adamw_step_batched(None, 0, ctypes.byref(h), 1, None) == 0         # nothing to do
+    arr[1].n = -1
+    assert lib.adamw_step_batched(arr, 2, ctypes.byref(h), 1, None) == 1
+    arr[1].n = 0                                                                   # empty: skipped
+    arr[0].n = 0
+    assert lib.adamw_step_batched(arr, 2, ctypes.byref(h), 1, None) == 0
+    arr[0].n = arr[1].n = 256
+    arr[1].v = (1 << 24) + 12290
+    assert lib.adamw_step_batched(arr, 2, ctypes.byref(h), 1, None) == 3          # misaligned
+    arr[1].v = (1 << 20) + 8192 + 512                                             # inside tensor 0's m
+    assert lib.adamw_step_batched(arr, 2, ctypes.byref(h), 1, None) == 1
+
+
 def test_graph_argument_validation(built):
     lib = built
     P = ctypes.c_void_p
