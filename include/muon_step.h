@@ -300,7 +300,9 @@ typedef struct {
  *     vector path for that tensor;
  *   - no buffer of one tensor may overlap a buffer of another;
  *   - n == 0 tensors are skipped; count == 0 is a no-op.
- * Errors as adamw_step's; nothing is enqueued when one tensor fails a check. */
+ * Errors as adamw_step's; nothing is enqueued when one tensor fails a check.
+ * Like adamw_step, it enqueues kernels only (the tensor table travels as
+ * kernel parameters), so a caller may capture it in a CUDA graph. */
 muon_status_t adamw_step_batched(const adamw_tensor_t* tensors, int64_t count,
                                  const adamw_hparams_t* hp, int64_t step, void* stream);
 

@@ -13,7 +13,8 @@ the oracle.  Covered here:
   * several workspace chunks, the gradient guard (a replay over a NaN
     gradient skips the step and reports MUON_STEP_SKIPPED);
   * more matrices than one record upload carries (several upload launches);
-  * a capture made by the caller (torch.cuda.graph) around MuonBatch.step;
+  * a capture made by the caller (torch.cuda.graph) around MuonBatch.step,
+    and around adamw_step_batched;
   * the launch count and timing rules of captured launches.
 """
 import numpy as np
@@ -208,3 +209,27 @@ def test_captured_launches_are_counted_per_replay_and_never_timed(lib):
         graph.destroy()
     finally:
         m.muon_set_timing(0)
+
+
+def test_caller_capture_of_batched_adamw(lib):
+    """adamw_step_batched enqueues kernels only (its tensor table is a kernel
+    parameter), so a graph captured by the caller replays the same update."""
+    gen = torch.Generator(device=DEV).manual_seed(37)
+    sizes = [5000, 1, 333, 1 << 16]
+    quads = [tuple(torch.randn(n, device=DEV, generator=gen).abs() * 1e-3 for _ in range(4)) for n in sizes]
+    twins = [tuple(x.clone() for x in q) for q in quads]
+    hp = m.AdamwHparams()
+    m.adamw_step_batched(quads, hp, step=7)   # warm-up outside the capture
+    m.adamw_step_batched(twins, hp, step=7)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cg, stream=side):
+        m.adamw_step_batched(quads, hp, step=7, stream=side)
+    for _ in range(2):
+        cg.replay()
+        m.adamw_step_batched(twins, hp, step=7)
+    torch.cuda.synchronize()
+    for a, b in zip(quads, twins):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
