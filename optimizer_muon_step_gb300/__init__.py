@@ -15,6 +15,7 @@ Functions keep the C names:
     muon_workspace_bytes_per_matrix(rows, cols)
     muon_workspace_size(shapes, budget_bytes)
     muon_query_status(workspace, stream=None)
+    MuonAdamW(muon_params, adamw_params, muon_hp, adamw_hp): a torch.optim.Optimizer
     muon_step_graph_create / _launch / _destroy (through MuonBatch.capture)
 """
 from __future__ import annotations
@@ -540,3 +541,11 @@ class MuonGraph:
             self.destroy()
         except Exception:
             pass
+
+
+def __getattr__(name):
+    # the torch.optim.Optimizer over this library (imports torch)
+    if name == "MuonAdamW":
+        from .optim import MuonAdamW
+        return MuonAdamW
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")
