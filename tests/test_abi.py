@@ -284,7 +284,8 @@ def test_graph_without_device_reports_no_device(built):
 
 def test_library_never_loads_the_oracle(built):
     # the product path has no reference to the oracle
-    for path in ("optimizer_muon_step_gb300/__init__.py", "optimizer_muon_step_gb300/build.py"):
+    for path in ("optimizer_muon_step_gb300/__init__.py", "optimizer_muon_step_gb300/build.py",
+                 "optimizer_muon_step_gb300/optim.py"):
         src = open(os.path.join(ROOT, path)).read()
         assert "oracle" not in src.replace("no CPU or PyTorch fallback", "")
     for name in os.listdir(os.path.join(ROOT, "optimizer_muon_step_gb300", "csrc")):
