@@ -6,6 +6,7 @@ import os
 import re
 
 import numpy as np
+import torch
 import pytest
 
 import oracle
@@ -290,3 +291,12 @@ def test_library_never_loads_the_oracle(built):
         assert "oracle" not in src.replace("no CPU or PyTorch fallback", "")
     for name in os.listdir(os.path.join(ROOT, "optimizer_muon_step_gb300", "csrc")):
         assert "oracle" not in open(os.path.join(ROOT, "optimizer_muon_step_gb300", "csrc", name)).read()
+
+
+def test_optimizer_class_checks_its_parameters():
+    """MuonAdamW takes fp32 CUDA parameters only and refuses an empty list
+    (checked on the host, before any library call)."""
+    with pytest.raises(TypeError):
+        m.MuonAdamW([torch.zeros(4, 4)], [])            # a CPU tensor
+    with pytest.raises(ValueError):
+        m.MuonAdamW([], [])
