@@ -300,3 +300,23 @@ def test_optimizer_class_checks_its_parameters():
         m.MuonAdamW([torch.zeros(4, 4)], [])            # a CPU tensor
     with pytest.raises(ValueError):
         m.MuonAdamW([], [])
+
+
+@pytest.mark.skipif(cuda_available(), reason="checks the no-device path")
+def test_fp16_gradient_dtype_rules(built):
+    """MUON_F16 gradients need 2-byte alignment only (like bf16): a G at an
+    odd 2-byte offset passes the host checks (the call then reports that no
+    device is current), an odd address is MUON_ERR_MISALIGNED, and an
+    unknown dtype is MUON_ERR_UNSUPPORTED_DTYPE."""
+    lib = built
+    arr = (m.MuonMatrix * 1)()
+    arr[0].W, arr[0].M = 1024, 4096
+    arr[0].rows, arr[0].cols = 4, 4
+    arr[0].g_dtype = m.MUON_F16
+    ws = ctypes.c_void_p(1 << 20)
+    arr[0].G = 8194                       # 2-byte aligned only
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(_hp()), ws, 1 << 20, None) == 7
+    arr[0].G = 8195
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(_hp()), ws, 1 << 20, None) == 3
+    arr[0].g_dtype = 3
+    assert lib.muon_step_batched(arr, 1, ctypes.byref(_hp()), ws, 1 << 20, None) == 2
