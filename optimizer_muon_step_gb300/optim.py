@@ -12,6 +12,8 @@ muon_step_batched and adamw_step_batched.  No arithmetic runs in Python.
 """
 from __future__ import annotations
 
+import dataclasses
+
 import torch
 
 from . import (AdamwHparams, MuonHparams, adamw_step_batched, allocate_workspace, muon_step_batched,
@@ -22,15 +24,20 @@ class MuonAdamW(torch.optim.Optimizer):
     """Muon on `muon_params` (fp32, 2-D; gradients fp32, bf16 or fp16) and
     AdamW on `adamw_params` (fp32, any shape, fp32 gradients).
 
-    `muon_hp` / `adamw_hp` hold the hyper-parameters and may be changed
-    between steps (a learning-rate schedule sets ``opt.muon_hp.lr``).
-    Parameters without a gradient are skipped.  AdamW's bias correction
-    uses each parameter's own step count."""
+    Each part's ``lr`` and ``weight_decay`` live in its param group (group 0
+    Muon, group 1 AdamW, when both are given), so torch.optim.lr_scheduler
+    schedules work as usual; they start from `muon_hp` / `adamw_hp`, which
+    hold the other hyper-parameters.  Parameters without a gradient are
+    skipped.  AdamW's bias correction uses each parameter's own step count."""
 
     def __init__(self, muon_params, adamw_params, muon_hp: MuonHparams | None = None,
                  adamw_hp: AdamwHparams | None = None, budget_bytes: int = 16 << 30):
-        groups = [{"params": list(muon_params), "kind": "muon"},
-                  {"params": list(adamw_params), "kind": "adamw"}]
+        muon_hp = muon_hp if muon_hp is not None else MuonHparams()
+        adamw_hp = adamw_hp if adamw_hp is not None else AdamwHparams()
+        groups = [{"params": list(muon_params), "kind": "muon", "lr": muon_hp.lr,
+                   "weight_decay": muon_hp.weight_decay},
+                  {"params": list(adamw_params), "kind": "adamw", "lr": adamw_hp.lr,
+                   "weight_decay": adamw_hp.weight_decay}]
         groups = [g for g in groups if g["params"]]
         if not groups:
             raise ValueError("no parameters")
@@ -41,8 +48,8 @@ class MuonAdamW(torch.optim.Optimizer):
                     raise TypeError("parameters must be fp32 CUDA tensors")
                 if g["kind"] == "muon" and p.dim() != 2:
                     raise ValueError("Muon parameters must be 2-D matrices")
-        self.muon_hp = muon_hp if muon_hp is not None else MuonHparams()
-        self.adamw_hp = adamw_hp if adamw_hp is not None else AdamwHparams()
+        self.muon_hp = muon_hp
+        self.adamw_hp = adamw_hp
         self.budget_bytes = int(budget_bytes)
         self._workspace = None
 
@@ -57,12 +64,14 @@ class MuonAdamW(torch.optim.Optimizer):
             if not params:
                 continue
             if group["kind"] == "muon":
-                self._muon(params)
+                hp = dataclasses.replace(self.muon_hp, lr=group["lr"], weight_decay=group["weight_decay"])
+                self._muon(params, hp)
             else:
-                self._adamw(params)
+                hp = dataclasses.replace(self.adamw_hp, lr=group["lr"], weight_decay=group["weight_decay"])
+                self._adamw(params, hp)
         return loss
 
-    def _muon(self, params):
+    def _muon(self, params, hp):
         W, G, M = [], [], []
         for p in params:
             st = self.state[p]
@@ -75,9 +84,9 @@ class MuonAdamW(torch.optim.Optimizer):
         if self._workspace is None or self._workspace.numel() < need:
             self._workspace = None
             self._workspace = allocate_workspace(need, W[0].device)
-        muon_step_batched(W, G, M, self.muon_hp, workspace=self._workspace)
+        muon_step_batched(W, G, M, hp, workspace=self._workspace)
 
-    def _adamw(self, params):
+    def _adamw(self, params, hp):
         by_step = {}
         for p in params:
             st = self.state[p]
@@ -92,4 +101,4 @@ class MuonAdamW(torch.optim.Optimizer):
             by_step.setdefault(st["step"], []).append(
                 (p.view(-1), g.contiguous().view(-1), st["exp_avg"].view(-1), st["exp_avg_sq"].view(-1)))
         for t, quads in sorted(by_step.items()):
-            adamw_step_batched(quads, self.adamw_hp, step=t)
+            adamw_step_batched(quads, hp, step=t)

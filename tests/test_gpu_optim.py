@@ -92,3 +92,31 @@ def test_state_dict_round_trip_resumes_bit_for_bit(lib, tmp_path):
     resumed.step()
     for a, b in zip(mu + ad, mu2 + ad2):
         assert torch.equal(a.detach(), b.detach())
+
+
+def test_lr_scheduler_drives_both_parts(lib):
+    """lr lives in the param groups, so a torch scheduler sets it: after one
+    LambdaLR step (factor 0.5) the second step uses half of each part's lr."""
+    mu, ad = make_params(93)
+    opt = m.MuonAdamW(mu, ad, m.MuonHparams(lr=0.02), m.AdamwHparams(lr=1e-3))
+    sched = torch.optim.lr_scheduler.LambdaLR(opt, lambda k: 0.5 ** k)
+    set_grads(mu + ad, seed=301)
+    opt.step()
+    sched.step()
+    assert [g["lr"] for g in opt.param_groups] == [0.01, 5e-4]
+    M1 = [opt.state[p]["momentum_buffer"].cpu().numpy() for p in mu]
+    st = [(opt.state[p]["exp_avg"].cpu().numpy().reshape(-1), opt.state[p]["exp_avg_sq"].cpu().numpy().reshape(-1))
+          for p in ad]
+    set_grads(mu + ad, seed=302)
+    W0 = [p.detach().cpu().numpy() for p in mu]
+    G0 = [p.grad.cpu().numpy() for p in mu]
+    P0 = [p.detach().cpu().numpy().reshape(-1) for p in ad]
+    g0 = [p.grad.cpu().numpy().reshape(-1) for p in ad]
+    opt.step()
+    for i, p in enumerate(mu):
+        oW, _, _, _ = oracle.muon_step_matrix(W0[i], G0[i], M1[i], oracle.MuonConfig(lr=0.01))
+        dW = p.detach().cpu().numpy().astype(np.float64) - W0[i]
+        assert rel_fro(dW, oW.astype(np.float64) - W0[i]) < TOL
+    for i, p in enumerate(ad):
+        rp, _, _ = oracle.adamw_step(P0[i], g0[i], st[i][0], st[i][1], oracle.AdamwConfig(lr=5e-4), t=2)
+        assert np.array_equal(p.detach().cpu().numpy().reshape(-1), rp)
