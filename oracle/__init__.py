@@ -101,6 +101,16 @@ def _load():
             lib.oracle_newton_schulz_table.restype = ctypes.c_int
             lib.oracle_newton_schulz_scaled.argtypes = [P, i64, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_float]
             lib.oracle_newton_schulz_scaled.restype = ctypes.c_int
+            lib.oracle_newton_schulz_ex.argtypes = [P, i64, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_float,
+                                                    ctypes.c_int]
+            lib.oracle_newton_schulz_ex.restype = ctypes.c_int
+            lib.oracle_matmul.argtypes = [P, P, P, i64, i64, i64, ctypes.c_int]
+            lib.oracle_matmul.restype = None
+            lib.oracle_normalize_cast_after.argtypes = [P, i64, i64, ctypes.c_float, P]
+            lib.oracle_normalize_cast_after.restype = ctypes.c_float
+            lib.oracle_muon_step_matrix_ex.argtypes = [P, P, P, i64, i64, P, ctypes.c_float, ctypes.c_int,
+                                                       ctypes.c_int, ctypes.c_int, P, P]
+            lib.oracle_muon_step_matrix_ex.restype = ctypes.c_int
             lib.oracle_update_scale.argtypes = [i64, i64, ctypes.c_float, ctypes.c_int]
             lib.oracle_update_scale.restype = ctypes.c_float
             lib.oracle_adamw_step.argtypes = [P, P, P, P, i64, P, i64]
@@ -158,20 +168,37 @@ QUINTIC = (3.4445, -4.7750, 2.0315)
 CUBIC = (1.5, -0.5, 0.0)  # [OPT] section 4.2: X <- (3X - X X^T X) / 2
 
 
-def newton_schulz(X, steps=5, coeffs=QUINTIC, emulate_bf16=True, x_scale=1.0) -> np.ndarray:
+def matmul(A, B, acc32=False) -> np.ndarray:
+    """A @ B with every element summed in ascending k: in fp64, or with
+    acc32 in fp32 (each product and each partial sum rounded to fp32)."""
+    A = np.ascontiguousarray(A, dtype=np.float64)
+    B = np.ascontiguousarray(B, dtype=np.float64)
+    if A.ndim != 2 or B.ndim != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("matmul expects M x K and K x N arrays")
+    C = np.empty((A.shape[0], B.shape[1]), dtype=np.float64)
+    _load().oracle_matmul(_ptr(A), _ptr(B), _ptr(C), A.shape[0], A.shape[1], B.shape[1], 1 if acc32 else 0)
+    return C
+
+
+def newton_schulz(X, steps=5, coeffs=QUINTIC, emulate_bf16=True, x_scale=1.0, acc32=False) -> np.ndarray:
     """Run the NS iteration on the wide matrix x_scale * X (rows <= cols).
 
     coeffs: one (a, b, c) for every step, or a sequence of `steps` triples.
     emulate_bf16=True: X must hold bf16 values; A, B and each new X are
     rounded to bf16 at the GPU's storage points, and x_scale is applied in
     fp32 inside the first step.  emulate_bf16=False: pure fp64, for the
-    closed-form checks."""
+    closed-form checks.  acc32 (with emulate_bf16): the products accumulate
+    in fp32 instead of fp64 -- a second, equally faithful evaluation, used to
+    measure how far such evaluations lie apart."""
     X = np.array(X, dtype=np.float64, order="C", copy=True)
     if X.ndim != 2 or X.shape[0] > X.shape[1]:
         raise ValueError("newton_schulz expects a wide 2-D matrix")
+    if acc32 and not emulate_bf16:
+        raise ValueError("acc32 applies to the bf16-emulating iteration only")
     table = coeff_table(coeffs, steps)
-    rc = _load().oracle_newton_schulz_scaled(_ptr(X), X.shape[0], X.shape[1], int(steps),
-                                             _ptr(table), 1 if emulate_bf16 else 0, float(x_scale))
+    rc = _load().oracle_newton_schulz_ex(_ptr(X), X.shape[0], X.shape[1], int(steps),
+                                         _ptr(table), 1 if emulate_bf16 else 0, float(x_scale),
+                                         1 if acc32 else 0)
     if rc:
         raise RuntimeError(f"oracle_newton_schulz failed ({rc})")
     return X
@@ -226,13 +253,16 @@ class MuonConfig:
         return h
 
 
-def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig(), g_scale: float = 1.0, scale_g: bool = False):
+def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig(), g_scale: float = 1.0, scale_g: bool = False,
+                     acc32: bool = False, cast_after_scale: bool = False):
     """One Muon step on one matrix.
 
     W, M: fp32 (rows x cols).  G: fp32 values (a bf16 gradient is passed as
     its exact fp32 widening).  Returns (W_new, M_new, X0, O) with X0 and O in
     the wide orientation (min(rows,cols) x max(rows,cols)); inputs are not
-    modified."""
+    modified.  acc32 / cast_after_scale select the spread variants: NS
+    products accumulated in fp32, and X0 = bf16(u * s) run unscaled instead
+    of X0 = bf16(u) with s applied inside the first NS step."""
     W = np.array(W, dtype=np.float32, order="C", copy=True)
     M = np.array(M, dtype=np.float32, order="C", copy=True)
     G = np.ascontiguousarray(G, dtype=np.float32)
@@ -243,10 +273,11 @@ def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig(), g_scale: float = 1.
     X0 = np.empty((mp, np_), dtype=np.float32)
     O = np.empty((mp, np_), dtype=np.float32)
     h = hp.c_struct()
-    rc = _load().oracle_muon_step_matrix_scaled(_ptr(W), _ptr(G), _ptr(M), rows, cols,
-                                                ctypes.byref(h), float(g_scale),
-                                                1 if g_scale is not None and scale_g else 0,
-                                                _ptr(X0), _ptr(O))
+    rc = _load().oracle_muon_step_matrix_ex(_ptr(W), _ptr(G), _ptr(M), rows, cols,
+                                            ctypes.byref(h), float(g_scale),
+                                            1 if g_scale is not None and scale_g else 0,
+                                            1 if acc32 else 0, 1 if cast_after_scale else 0,
+                                            _ptr(X0), _ptr(O))
     if rc:
         raise RuntimeError(f"oracle_muon_step_matrix failed ({rc})")
     return W, M, X0, O
@@ -263,13 +294,15 @@ def momentum(G, M, mu=0.95, nesterov=True):
     return M, u
 
 
-def normalize(u, eps=1e-7):
+def normalize(u, eps=1e-7, cast_after_scale=False):
     """Steps 3-4: returns (X0 = bf16(u) wide as float values, s); the
-    normalised NS input is s * X0, s applied inside the first NS step."""
+    normalised NS input is s * X0, s applied inside the first NS step.
+    cast_after_scale: X0 = bf16(u * s) instead, the NS input itself."""
     u = np.ascontiguousarray(u, dtype=np.float32)
     rows, cols = u.shape
     X0 = np.empty((min(rows, cols), max(rows, cols)), dtype=np.float64)
-    s = _load().oracle_normalize(_ptr(u), rows, cols, float(eps), _ptr(X0))
+    fn = _load().oracle_normalize_cast_after if cast_after_scale else _load().oracle_normalize
+    s = fn(_ptr(u), rows, cols, float(eps), _ptr(X0))
     return X0.astype(np.float32), float(s)
 
 

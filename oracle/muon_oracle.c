@@ -24,6 +24,11 @@
  *   - every matrix product is accumulated in fp64 in ascending k order, then
  *     rounded once to fp32; bf16 rounding is round-to-nearest-even of that
  *     fp32 value (see oracle_bf16_from_f32).
+ *   - two variants exist only to measure how far two equally faithful bf16
+ *     evaluations of the step lie apart (the iteration is not unique once
+ *     it is rounded): products accumulated in fp32 instead of fp64
+ *     (acc32), and the cast to bf16 taken after the normalisation instead
+ *     of before it (cast_after_scale).  The pages fix neither choice.
  */
 #include <math.h>
 #include <stdint.h>
@@ -106,6 +111,50 @@ static void matmul_f64(const double* A, const double* B, double* C,
     }
 }
 
+/* The same product with each C[i][j] accumulated in fp32 instead: in
+ * ascending k, every product a*b rounded to fp32 and every partial sum
+ * rounded to fp32 (for bf16 operands the products are exact in fp32; only
+ * the additions round).  The result is stored as the fp64 value of that
+ * fp32 sum. */
+static void matmul_f32acc(const double* A, const double* B, double* C,
+                          int64_t M, int64_t K, int64_t N)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        float* c = (float*)malloc(sizeof(float) * (N > 0 ? N : 1));
+        for (int64_t j = 0; j < N; ++j)
+            c[j] = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            const float a = (float)A[i * K + k];
+            const double* b = B + k * N;
+            for (int64_t j = 0; j < N; ++j) {
+                const float prod = a * (float)b[j];
+                c[j] = c[j] + prod;
+            }
+        }
+        for (int64_t j = 0; j < N; ++j)
+            C[i * N + j] = (double)c[j];
+        free(c);
+    }
+}
+
+static void matmul(const double* A, const double* B, double* C,
+                   int64_t M, int64_t K, int64_t N, int acc32)
+{
+    if (acc32)
+        matmul_f32acc(A, B, C, M, K, N);
+    else
+        matmul_f64(A, B, C, M, K, N);
+}
+
+/* C = A B (M x K times K x N, row-major fp64 arrays), accumulated in fp64
+ * (acc32 == 0) or fp32 (acc32 != 0) as above. */
+void oracle_matmul(const double* A, const double* B, double* C,
+                   int64_t M, int64_t K, int64_t N, int acc32)
+{
+    matmul(A, B, C, M, K, N, acc32);
+}
+
 static void transpose_f64(const double* X, double* XT, int64_t R, int64_t C)
 {
     for (int64_t r = 0; r < R; ++r)
@@ -139,10 +188,14 @@ static void transpose_f64(const double* X, double* XT, int64_t R, int64_t C)
  *   (a factor of 1 is exact, so later steps are the plain iteration).  With
  *   no steps the result is bf16( fl32(x_scale * X) ).
  * emulate_bf16 == 0: everything stays in fp64 (used to check the iteration
- *   against its singular-value closed form). */
-int oracle_newton_schulz_scaled(double* X, int64_t rows, int64_t cols, int steps,
-                                const float* coeffs, int emulate_bf16, float x_scale)
+ *   against its singular-value closed form).
+ * acc32 != 0 (with emulate_bf16 only): the three products are accumulated
+ *   in fp32 (matmul_f32acc) instead of fp64; the spread variant. */
+int oracle_newton_schulz_ex(double* X, int64_t rows, int64_t cols, int steps,
+                            const float* coeffs, int emulate_bf16, float x_scale, int acc32)
 {
+    if (acc32 && !emulate_bf16)
+        return 1;
     if (rows <= 0 || cols <= 0 || steps < 0 || rows > cols || (steps > 0 && !coeffs))
         return 1;
     if (steps == 0) {
@@ -164,7 +217,7 @@ int oracle_newton_schulz_scaled(double* X, int64_t rows, int64_t cols, int steps
         const float xs = s == 0 ? x_scale : 1.0f;  /* input scale, first step only */
         /* A = (xs X)(xs X)^T */
         transpose_f64(X, XT, rows, cols);
-        matmul_f64(X, XT, A, rows, cols, rows);
+        matmul(X, XT, A, rows, cols, rows, acc32);
         if (emulate_bf16) {
             const float xs2 = xs * xs;
             for (int64_t i = 0; i < rows * rows; ++i)
@@ -174,7 +227,7 @@ int oracle_newton_schulz_scaled(double* X, int64_t rows, int64_t cols, int steps
                 A[i] *= (double)xs * (double)xs;
         }
         /* B = b A + c A A */
-        matmul_f64(A, A, AA, rows, rows, rows);
+        matmul(A, A, AA, rows, rows, rows, acc32);
         for (int64_t i = 0; i < rows * rows; ++i) {
             if (emulate_bf16) {
                 float t1 = b * (float)A[i];
@@ -185,7 +238,7 @@ int oracle_newton_schulz_scaled(double* X, int64_t rows, int64_t cols, int steps
             }
         }
         /* X = a (xs X) + B (xs X) */
-        matmul_f64(Bm, X, BX, rows, rows, cols);
+        matmul(Bm, X, BX, rows, rows, cols, acc32);
         const float axs = a * xs;
         for (int64_t i = 0; i < rows * cols; ++i) {
             if (emulate_bf16) {
@@ -199,6 +252,12 @@ int oracle_newton_schulz_scaled(double* X, int64_t rows, int64_t cols, int steps
     }
     free(XT); free(A); free(AA); free(Bm); free(BX);
     return 0;
+}
+
+int oracle_newton_schulz_scaled(double* X, int64_t rows, int64_t cols, int steps,
+                                const float* coeffs, int emulate_bf16, float x_scale)
+{
+    return oracle_newton_schulz_ex(X, rows, cols, steps, coeffs, emulate_bf16, x_scale, 0);
 }
 
 /* The iteration on X itself (input scale 1). */
@@ -301,6 +360,27 @@ float oracle_normalize(const float* u, int64_t rows, int64_t cols, float eps, do
     return s;
 }
 
+/* Steps 3-4 under the other reading of where the cast falls: the
+ * normalised look-ahead itself is cast, X0 = bf16(fl32(u * s)) (wide, as
+ * above), and the NS iteration then runs on X0 unscaled.  s is the same
+ * fp32 value oracle_normalize returns; so is the return value. */
+float oracle_normalize_cast_after(const float* u, int64_t rows, int64_t cols, float eps, double* X0)
+{
+    const float s = oracle_normalize(u, rows, cols, eps, X0);
+    const int transposed = rows > cols;
+    const int64_t np = transposed ? rows : cols;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            const float scaled = u[r * cols + c] * s;
+            double x0 = bf16_round(scaled);
+            if (transposed)
+                X0[c * np + r] = x0;
+            else
+                X0[r * np + c] = x0;
+        }
+    return s;
+}
+
 /* The update's scale factor, computed in fp64 and rounded to fp32:
  *   mode 0: rms_scale * sqrt(max(rows, cols)) -- the update RMS matches
  *           AdamW's 0.2-0.4 ([K2] section 3.1);
@@ -374,15 +454,21 @@ void oracle_step_stats(const float* u, const float* O, int64_t rows, int64_t col
  *   G   gradient, fp32 values (a bf16 gradient is passed already widened:
  *       the widening is exact)
  *   M   fp32 momentum, updated in place
- *   X0  optional out: the bf16 look-ahead the NS input is s times (wide,
+ *   acc32             the NS products accumulate in fp32, not fp64
+ *   cast_after_scale  X0 = bf16(u * s) and NS runs on it unscaled
+ *                     (oracle_normalize_cast_after), instead of X0 =
+ *                     bf16(u) with s applied inside the first NS step
+ *   X0  optional out: the bf16 NS input before any in-step scale (wide,
  *       float values)
  *   O   optional out: the NS output (wide, float values)
- * Returns 0 on success. */
-int oracle_muon_step_matrix_scaled(float* W, const float* G, float* M,
-                                   int64_t rows, int64_t cols,
-                                   const oracle_muon_hparams* hp,
-                                   float g_scale, int scale_g,
-                                   float* X0_out, float* O_out)
+ * The two flags select the spread variants; (0, 0) is the library's
+ * arithmetic.  Returns 0 on success. */
+int oracle_muon_step_matrix_ex(float* W, const float* G, float* M,
+                               int64_t rows, int64_t cols,
+                               const oracle_muon_hparams* hp,
+                               float g_scale, int scale_g,
+                               int acc32, int cast_after_scale,
+                               float* X0_out, float* O_out)
 {
     if (rows <= 0 || cols <= 0 || !hp)
         return 1;
@@ -397,7 +483,8 @@ int oracle_muon_step_matrix_scaled(float* W, const float* G, float* M,
         return 2;
     }
     oracle_momentum_scaled(G, M, u, n, hp->momentum, hp->nesterov, g_scale, scale_g);
-    const float s = oracle_normalize(u, rows, cols, hp->norm_eps, X);
+    const float s = cast_after_scale ? oracle_normalize_cast_after(u, rows, cols, hp->norm_eps, X)
+                                     : oracle_normalize(u, rows, cols, hp->norm_eps, X);
     if (X0_out)
         for (int64_t i = 0; i < n; ++i)
             X0_out[i] = (float)X[i];
@@ -415,7 +502,7 @@ int oracle_muon_step_matrix_scaled(float* W, const float* G, float* M,
         }
         coeffs = table;
     }
-    int rc = oracle_newton_schulz_scaled(X, mp, np, hp->ns_steps, coeffs, 1, s);
+    int rc = oracle_newton_schulz_ex(X, mp, np, hp->ns_steps, coeffs, 1, cast_after_scale ? 1.0f : s, acc32);
     if (rc) {
         free(u); free(X); free(O);
         return 10 + rc;
@@ -427,6 +514,17 @@ int oracle_muon_step_matrix_scaled(float* W, const float* G, float* M,
     oracle_final_update(W, O, rows, cols, hp->lr, hp->weight_decay, hp->rms_scale, hp->scale_mode);
     free(u); free(X); free(O);
     return 0;
+}
+
+/* The step as the library computes it: fp64 products, the look-ahead cast
+ * before the normalisation. */
+int oracle_muon_step_matrix_scaled(float* W, const float* G, float* M,
+                                   int64_t rows, int64_t cols,
+                                   const oracle_muon_hparams* hp,
+                                   float g_scale, int scale_g,
+                                   float* X0_out, float* O_out)
+{
+    return oracle_muon_step_matrix_ex(W, G, M, rows, cols, hp, g_scale, scale_g, 0, 0, X0_out, O_out);
 }
 
 int oracle_muon_step_matrix(float* W, const float* G, float* M,

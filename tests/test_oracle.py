@@ -445,6 +445,109 @@ def test_stage_functions_compose_to_the_step():
     assert s > 0 and abs(np.linalg.norm(u.astype(np.float64)) * s - 1) < 1e-6
 
 
+# --------------------------------------------------------------------------
+# Spread variants: the same step evaluated with fp32-accumulated products,
+# or with the cast to bf16 after the normalisation.  They measure how far
+# two faithful bf16 evaluations lie apart; each is pinned on its own.
+# --------------------------------------------------------------------------
+
+def test_fp32_accumulation_is_ascending_and_rounds_every_sum():
+    """1 + 2^-24 + 2^-24: summed in fp32 in ascending k, each addition ties
+    back to 1 (round half to even), so the result is exactly 1; in fp64 it is
+    1 + 2^-23.  Summed in the other order fp32 gives 1 + 2^-23 as well, so
+    the pair pins both the precision and the order."""
+    x = np.array([[1.0, 2.0 ** -12, 2.0 ** -12]])
+    assert oracle.matmul(x, x.T)[0, 0] == 1.0 + 2.0 ** -23
+    assert oracle.matmul(x, x.T, acc32=True)[0, 0] == 1.0
+    r = x[:, ::-1].copy()
+    assert oracle.matmul(r, r.T, acc32=True)[0, 0] == 1.0 + 2.0 ** -23
+
+
+def test_fp32_accumulation_exact_on_small_integers():
+    """Products and sums of small integers are exact in fp32: both
+    accumulations give numpy's integer product (a transposed or misindexed
+    operand would not)."""
+    rng = np.random.default_rng(21)
+    A = rng.integers(-8, 9, size=(7, 33))
+    B = rng.integers(-8, 9, size=(33, 5))
+    ref = (A @ B).astype(np.float64)
+    assert np.array_equal(oracle.matmul(A, B), ref)
+    assert np.array_equal(oracle.matmul(A, B, acc32=True), ref)
+
+
+def test_ns_fp32_accumulation_exact_on_integer_input():
+    """One NS step with (a, b, c) = (1, 1, 1) on a small {-1, 0, 1} matrix
+    stays within the integers bf16 holds exactly (|values| < 256), so both
+    accumulations must return X + (A + A A) X with A = X X^T, computed here in
+    integer arithmetic."""
+    rng = np.random.default_rng(22)
+    X = rng.integers(-1, 2, size=(3, 5))
+    A = X @ X.T
+    ref = (X + (A + A @ A) @ X).astype(np.float64)
+    assert np.abs(ref).max() < 256
+    for acc32 in (False, True):
+        got = oracle.newton_schulz(X.astype(np.float64), steps=1, coeffs=(1.0, 1.0, 1.0), acc32=acc32)
+        assert np.array_equal(got, ref), acc32
+
+
+def test_ns_fp32_accumulation_stays_within_bf16_noise():
+    """The fp32-accumulating iteration differs from the fp64 one only where a
+    sum lands near a bf16 rounding boundary: on a well-conditioned input the
+    two outputs are close but not identical."""
+    from workloads import ns_input
+    X = ns_input(96, 256, seed=4).float().numpy()
+    a = oracle.newton_schulz(X)
+    b = oracle.newton_schulz(X, acc32=True)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(a)
+    assert 0 < rel < 1e-2
+
+
+@pytest.mark.parametrize("shape", [(16, 64), (64, 16)])
+def test_cast_after_scale_equals_cast_before_for_power_of_two_norms(shape):
+    """When s = 1/||u|| is a power of two (eps = 0, every |u| = 2^-6 over
+    1024 elements: ||u|| = 2^-1), scaling commutes with every rounding, so
+    the two readings of where the cast falls give bit-identical steps, in
+    both orientations.  The other reading applying s twice, or not at all,
+    would break this."""
+    rng = np.random.default_rng(23)
+    G = (rng.choice([-1.0, 1.0], size=shape) * 2.0 ** -6).astype(np.float32)
+    W = (rng.standard_normal(shape) * 0.02).astype(np.float32)
+    M = np.zeros(shape, np.float32)
+    hp = oracle.MuonConfig(momentum=0.0, norm_eps=0.0)    # u = G exactly
+    ref = oracle.muon_step_matrix(W, G, M, hp)
+    var = oracle.muon_step_matrix(W, G, M, hp, cast_after_scale=True)
+    assert np.array_equal(ref[0], var[0]) and np.array_equal(ref[3], var[3])
+    assert np.array_equal(var[2], ref[2] * np.float32(2.0))  # X0 = bf16(u s), s = 2
+
+
+def test_cast_after_scale_input_has_unit_norm():
+    """X0 = bf16(u s) is the normalised look-ahead itself: unit Frobenius
+    norm up to bf16 rounding (relative 2^-8 per element)."""
+    W, G, M = _inputs(48, 80, 9)
+    _, u = oracle.momentum(G, M)
+    X0, s = oracle.normalize(u, cast_after_scale=True)
+    assert abs(np.linalg.norm(X0.astype(np.float64)) - 1.0) < 2 ** -8
+    X0b, sb = oracle.normalize(u)
+    assert s == sb
+    # one rounding of u s, not the double rounding bf16(bf16(u) s)
+    assert np.array_equal(oracle.bf16_round(u * np.float32(s)), X0)
+    assert not np.array_equal(oracle.bf16_round(X0b * np.float32(s)), X0)
+
+
+def test_step_variants_route_through_the_staged_functions():
+    """Each variant of the step is the staged functions with that choice:
+    fp32 products in every NS stage, or the NS run unscaled on bf16(u s)."""
+    W, G, M = _inputs(40, 24, 10)
+    hp = oracle.MuonConfig()
+    _, u = oracle.momentum(G, M, hp.momentum, hp.nesterov)
+    X0, s = oracle.normalize(u)
+    O32 = oracle.newton_schulz(X0, hp.ns_steps, x_scale=s, acc32=True).astype(np.float32)
+    assert np.array_equal(oracle.muon_step_matrix(W, G, M, hp, acc32=True)[3], O32)
+    X0c, _ = oracle.normalize(u, cast_after_scale=True)
+    Oc = oracle.newton_schulz(X0c, hp.ns_steps).astype(np.float32)
+    assert np.array_equal(oracle.muon_step_matrix(W, G, M, hp, cast_after_scale=True)[3], Oc)
+
+
 
 # --------------------------------------------------------------------------
 # Next rows: per-step NS coefficients, the muP update scale, the gradient
