@@ -302,6 +302,20 @@ def test_optimizer_class_checks_its_parameters():
         m.MuonAdamW([], [])
 
 
+def test_optimizer_refuses_parameters_on_several_devices():
+    """The library reads every pointer on the current device, so one
+    optimizer's parameters must share a device (checked on the host)."""
+    from types import SimpleNamespace
+    from optimizer_muon_step_gb300.optim import common_device
+
+    on = lambda d: SimpleNamespace(device=torch.device(d))  # noqa: E731
+    assert common_device([on("cuda:1"), on("cuda:1")]) == torch.device("cuda:1")
+    with pytest.raises(ValueError):
+        common_device([on("cuda:0"), on("cuda:1")])
+    with pytest.raises(ValueError):
+        common_device([])
+
+
 @pytest.mark.skipif(cuda_available(), reason="checks the no-device path")
 def test_fp16_gradient_dtype_rules(built):
     """MUON_F16 gradients need 2-byte alignment only (like bf16): a G at an

@@ -94,6 +94,75 @@ def test_state_dict_round_trip_resumes_bit_for_bit(lib, tmp_path):
         assert torch.equal(a.detach(), b.detach())
 
 
+def test_rejected_adamw_gradient_leaves_the_state_alone(lib):
+    """An fp16 AdamW gradient is refused before any state changes: step
+    counts, m and v stay as they were, and the same step with a corrected
+    gradient then matches the oracle's first step."""
+    mu, ad = make_params(94)
+    opt = m.MuonAdamW([], ad, adamw_hp=m.AdamwHparams(lr=1e-3))
+    set_grads(ad, seed=401)
+    opt.step()
+    before = {p: (opt.state[p]["step"], opt.state[p]["exp_avg"].clone(), opt.state[p]["exp_avg_sq"].clone())
+              for p in ad}
+    set_grads(ad, seed=402)
+    good = ad[0].grad.clone()
+    ad[0].grad = good.half()
+    P0 = [p.detach().clone() for p in ad]
+    with pytest.raises(TypeError):
+        opt.step()
+    for p, p0 in zip(ad, P0):
+        assert opt.state[p]["step"] == before[p][0] == 1
+        assert torch.equal(opt.state[p]["exp_avg"], before[p][1])
+        assert torch.equal(opt.state[p]["exp_avg_sq"], before[p][2])
+        assert torch.equal(p.detach(), p0)
+    ad[0].grad = good
+    host = [(p.detach().cpu().numpy().reshape(-1), p.grad.cpu().numpy().reshape(-1),
+             before[p][1].cpu().numpy().reshape(-1), before[p][2].cpu().numpy().reshape(-1)) for p in ad]
+    opt.step()
+    for p, (p0, g0, m0, v0) in zip(ad, host):
+        rp, _, _ = oracle.adamw_step(p0, g0, m0, v0, oracle.AdamwConfig(lr=1e-3), t=2)
+        assert np.array_equal(p.detach().cpu().numpy().reshape(-1), rp)
+        assert opt.state[p]["step"] == 2
+
+
+def test_muon_gradient_layouts_and_a_skipped_parameter(lib):
+    """The Muon gradients the optimizer accepts besides contiguous fp32: a
+    transposed view (strided; made contiguous before the call) and an fp16
+    gradient (widened exactly).  A parameter without a gradient on one step
+    is skipped with its momentum kept, and on the next step continues from
+    that momentum.  All against the oracle."""
+    mu, _ = make_params(95)
+    opt = m.MuonAdamW(mu, [])
+    cfg = oracle.MuonConfig()
+    Mh = [np.zeros(s, np.float32) for s in MUON_SHAPES]
+    gen = torch.Generator(device=DEV).manual_seed(501)
+    for t in range(3):
+        grads = []
+        for i, (r, c) in enumerate(MUON_SHAPES):
+            g = torch.randn(c, r, device=DEV, generator=gen).t() * 1e-2    # a transposed view
+            if i == 1:
+                g = g.contiguous().half()                                  # fp16
+            grads.append(g)
+        skip = 2 if t == 1 else None                                       # no gradient on step 1
+        for i, p in enumerate(mu):
+            p.grad = None if i == skip else grads[i]
+        assert not grads[0].is_contiguous()
+        W0 = [p.detach().cpu().numpy() for p in mu]
+        M_before = [opt.state[p]["momentum_buffer"].clone() if p in opt.state else None for p in mu]
+        opt.step()
+        for i, p in enumerate(mu):
+            if i == skip:
+                assert np.array_equal(p.detach().cpu().numpy(), W0[i])
+                assert torch.equal(opt.state[p]["momentum_buffer"], M_before[i])
+                continue
+            G0 = grads[i].float().cpu().numpy()
+            oW, oM, _, _ = oracle.muon_step_matrix(W0[i], G0, Mh[i], cfg)
+            assert np.array_equal(opt.state[p]["momentum_buffer"].cpu().numpy(), oM), (t, i)
+            dW = p.detach().cpu().numpy().astype(np.float64) - W0[i]
+            assert rel_fro(dW, oW.astype(np.float64) - W0[i]) < TOL, (t, i)
+            Mh[i] = oM
+
+
 def test_lr_scheduler_drives_both_parts(lib):
     """lr lives in the param groups, so a torch scheduler sets it: after one
     LambdaLR step (factor 0.5) the second step uses half of each part's lr."""
