@@ -206,8 +206,10 @@ muon_status_t muon_step_batched_stats(const muon_matrix_t* mats, int64_t count,
  *     (e.g. up to 2048 x 5632), else MUON_ERR_WORKSPACE_TOO_SMALL and
  *     nothing is enqueued; larger call lists run in several passes;
  *   - the first call on a device resolves the scratch's device address
- *     (cudaGetSymbolAddress) with that device current; make that first
- *     call before any stream capture;
+ *     (cudaGetSymbolAddress) with that device current and keeps it for
+ *     the life of the process; make that first call before any stream
+ *     capture, and do not call this entry point again in a process that
+ *     has reset the device (cudaDeviceReset), whose kept address is stale;
  *   - all calls on a device share the one scratch, which keeps the previous
  *     call's contents (the step rewrites everything it reads, and clears its
  *     status word itself): calls that overlap on the GPU (other streams,
@@ -301,6 +303,9 @@ typedef struct {
  *   - no buffer of one tensor may overlap a buffer of another;
  *   - n == 0 tensors are skipped; count == 0 is a no-op.
  * Errors as adamw_step's; nothing is enqueued when one tensor fails a check.
+ * A launch error (MUON_ERR_CUDA) after the first launch leaves the tensors
+ * of the launches already enqueued (whole groups of 448, in array order)
+ * updated and the rest untouched; the call does not say which.
  * Like adamw_step, it enqueues kernels only (the tensor table travels as
  * kernel parameters), so a caller may capture it in a CUDA graph. */
 muon_status_t adamw_step_batched(const adamw_tensor_t* tensors, int64_t count,

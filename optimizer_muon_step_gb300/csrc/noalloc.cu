@@ -26,7 +26,11 @@ std::mutex g_mu;
 void* g_scratch_ptr[64] = {};
 
 // Resolves the device address of g_scratch for the current device, once per
-// device, with that device current.
+// device, with that device current, and keeps it for the life of the
+// process.  The address belongs to the device's primary context: after a
+// cudaDeviceReset (or anything else that destroys that context) the kept
+// address is stale, so this entry point must not be called again in that
+// process.
 muon_status_t scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MUON_ERR_NO_DEVICE;
