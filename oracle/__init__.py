@@ -164,41 +164,54 @@ def bf16_round(x) -> np.ndarray:
 # Newton-Schulz
 # --------------------------------------------------------------------------
 
+# How the NS products accumulate (the spread variants; ACC_FP64 is the
+# reference evaluation): fp64; fp32 with one rounding per addition; fp32 with
+# blocks of 16 products each added with one round-toward-zero.
+ACC_FP64, ACC_FP32, ACC_FP32_RZ16 = 0, 1, 2
+
 QUINTIC = (3.4445, -4.7750, 2.0315)
 CUBIC = (1.5, -0.5, 0.0)  # [OPT] section 4.2: X <- (3X - X X^T X) / 2
 
 
-def matmul(A, B, acc32=False) -> np.ndarray:
-    """A @ B with every element summed in ascending k: in fp64, or with
-    acc32 in fp32 (each product and each partial sum rounded to fp32)."""
+def matmul(A, B, accum=ACC_FP64) -> np.ndarray:
+    """A @ B with every element summed in ascending k: in fp64 (ACC_FP64), in
+    fp32 with each product and each partial sum rounded to nearest
+    (ACC_FP32), or in fp32 with each block of 16 products summed in fp64 and
+    added with one rounding toward zero (ACC_FP32_RZ16)."""
     A = np.ascontiguousarray(A, dtype=np.float64)
     B = np.ascontiguousarray(B, dtype=np.float64)
     if A.ndim != 2 or B.ndim != 2 or A.shape[1] != B.shape[0]:
         raise ValueError("matmul expects M x K and K x N arrays")
     C = np.empty((A.shape[0], B.shape[1]), dtype=np.float64)
-    _load().oracle_matmul(_ptr(A), _ptr(B), _ptr(C), A.shape[0], A.shape[1], B.shape[1], 1 if acc32 else 0)
+    _load().oracle_matmul(_ptr(A), _ptr(B), _ptr(C), A.shape[0], A.shape[1], B.shape[1], _accum(accum))
     return C
 
 
-def newton_schulz(X, steps=5, coeffs=QUINTIC, emulate_bf16=True, x_scale=1.0, acc32=False) -> np.ndarray:
+def _accum(accum) -> int:
+    if accum not in (ACC_FP64, ACC_FP32, ACC_FP32_RZ16):
+        raise ValueError("accum must be ACC_FP64, ACC_FP32 or ACC_FP32_RZ16")
+    return int(accum)
+
+
+def newton_schulz(X, steps=5, coeffs=QUINTIC, emulate_bf16=True, x_scale=1.0, accum=ACC_FP64) -> np.ndarray:
     """Run the NS iteration on the wide matrix x_scale * X (rows <= cols).
 
     coeffs: one (a, b, c) for every step, or a sequence of `steps` triples.
     emulate_bf16=True: X must hold bf16 values; A, B and each new X are
     rounded to bf16 at the GPU's storage points, and x_scale is applied in
     fp32 inside the first step.  emulate_bf16=False: pure fp64, for the
-    closed-form checks.  acc32 (with emulate_bf16): the products accumulate
-    in fp32 instead of fp64 -- a second, equally faithful evaluation, used to
-    measure how far such evaluations lie apart."""
+    closed-form checks.  accum (with emulate_bf16): how the products
+    accumulate (see matmul); the fp32 modes are equally faithful
+    evaluations, used to measure how far such evaluations lie apart."""
     X = np.array(X, dtype=np.float64, order="C", copy=True)
     if X.ndim != 2 or X.shape[0] > X.shape[1]:
         raise ValueError("newton_schulz expects a wide 2-D matrix")
-    if acc32 and not emulate_bf16:
-        raise ValueError("acc32 applies to the bf16-emulating iteration only")
+    if _accum(accum) != ACC_FP64 and not emulate_bf16:
+        raise ValueError("fp32 accumulation applies to the bf16-emulating iteration only")
     table = coeff_table(coeffs, steps)
     rc = _load().oracle_newton_schulz_ex(_ptr(X), X.shape[0], X.shape[1], int(steps),
                                          _ptr(table), 1 if emulate_bf16 else 0, float(x_scale),
-                                         1 if acc32 else 0)
+                                         _accum(accum))
     if rc:
         raise RuntimeError(f"oracle_newton_schulz failed ({rc})")
     return X
@@ -254,15 +267,16 @@ class MuonConfig:
 
 
 def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig(), g_scale: float = 1.0, scale_g: bool = False,
-                     acc32: bool = False, cast_after_scale: bool = False):
+                     accum: int = ACC_FP64, cast_after_scale: bool = False):
     """One Muon step on one matrix.
 
     W, M: fp32 (rows x cols).  G: fp32 values (a bf16 gradient is passed as
     its exact fp32 widening).  Returns (W_new, M_new, X0, O) with X0 and O in
     the wide orientation (min(rows,cols) x max(rows,cols)); inputs are not
-    modified.  acc32 / cast_after_scale select the spread variants: NS
-    products accumulated in fp32, and X0 = bf16(u * s) run unscaled instead
-    of X0 = bf16(u) with s applied inside the first NS step."""
+    modified.  accum / cast_after_scale select the spread variants: NS
+    products accumulated in fp32 (see matmul), and X0 = bf16(u * s) run
+    unscaled instead of X0 = bf16(u) with s applied inside the first NS
+    step."""
     W = np.array(W, dtype=np.float32, order="C", copy=True)
     M = np.array(M, dtype=np.float32, order="C", copy=True)
     G = np.ascontiguousarray(G, dtype=np.float32)
@@ -276,7 +290,7 @@ def muon_step_matrix(W, G, M, hp: MuonConfig = MuonConfig(), g_scale: float = 1.
     rc = _load().oracle_muon_step_matrix_ex(_ptr(W), _ptr(G), _ptr(M), rows, cols,
                                             ctypes.byref(h), float(g_scale),
                                             1 if g_scale is not None and scale_g else 0,
-                                            1 if acc32 else 0, 1 if cast_after_scale else 0,
+                                            _accum(accum), 1 if cast_after_scale else 0,
                                             _ptr(X0), _ptr(O))
     if rc:
         raise RuntimeError(f"oracle_muon_step_matrix failed ({rc})")

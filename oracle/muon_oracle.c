@@ -24,11 +24,15 @@
  *   - every matrix product is accumulated in fp64 in ascending k order, then
  *     rounded once to fp32; bf16 rounding is round-to-nearest-even of that
  *     fp32 value (see oracle_bf16_from_f32).
- *   - two variants exist only to measure how far two equally faithful bf16
+ *   - variants exist only to measure how far equally faithful bf16
  *     evaluations of the step lie apart (the iteration is not unique once
- *     it is rounded): products accumulated in fp32 instead of fp64
- *     (acc32), and the cast to bf16 taken after the normalisation instead
- *     of before it (cast_after_scale).  The pages fix neither choice.
+ *     it is rounded): products accumulated in fp32 instead of fp64, either
+ *     one rounded-to-nearest addition per product (ACC_FP32) or blocks of 16
+ *     products added to the fp32 sum with one round-toward-zero each
+ *     (ACC_FP32_RZ16, the way tensor-core fp32 accumulation behaves in
+ *     measurement); and the cast to bf16 taken after the normalisation
+ *     instead of before it (cast_after_scale).  The pages fix none of these
+ *     choices.
  */
 #include <math.h>
 #include <stdint.h>
@@ -138,21 +142,71 @@ static void matmul_f32acc(const double* A, const double* B, double* C,
     }
 }
 
-static void matmul(const double* A, const double* B, double* C,
-                   int64_t M, int64_t K, int64_t N, int acc32)
+/* x rounded to fp32 toward zero: the nearest-rounded fp32 value, moved one
+ * step towards zero when it lies farther from zero than x. */
+static float f32_toward_zero(double x)
 {
-    if (acc32)
+    float f = (float)x;
+    if (fabs((double)f) > fabs(x))
+        f = nextafterf(f, 0.0f);
+    return f;
+}
+
+/* The same product accumulated block-wise: the products of each run of 16
+ * consecutive k (ascending; the last run may be shorter) are summed in
+ * fp64, and each run's sum is added to the fp32 accumulator with one
+ * rounding toward zero, acc = rz32(acc + run).  For bf16 operands the fp64
+ * run sums are exact unless a run's products span more than 37 binades. */
+static void matmul_f32rz16(const double* A, const double* B, double* C,
+                           int64_t M, int64_t K, int64_t N)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        float* c = (float*)malloc(sizeof(float) * (N > 0 ? N : 1));
+        double* run = (double*)malloc(sizeof(double) * (N > 0 ? N : 1));
+        for (int64_t j = 0; j < N; ++j)
+            c[j] = 0.0f;
+        for (int64_t k0 = 0; k0 < K; k0 += 16) {
+            const int64_t k1 = k0 + 16 < K ? k0 + 16 : K;
+            for (int64_t j = 0; j < N; ++j)
+                run[j] = 0.0;
+            for (int64_t k = k0; k < k1; ++k) {
+                const double a = A[i * K + k];
+                const double* b = B + k * N;
+                for (int64_t j = 0; j < N; ++j)
+                    run[j] += a * b[j];
+            }
+            for (int64_t j = 0; j < N; ++j)
+                c[j] = f32_toward_zero((double)c[j] + run[j]);
+        }
+        for (int64_t j = 0; j < N; ++j)
+            C[i * N + j] = (double)c[j];
+        free(run);
+        free(c);
+    }
+}
+
+/* Accumulation modes of the products (see the header). */
+enum { ACC_FP64 = 0, ACC_FP32 = 1, ACC_FP32_RZ16 = 2 };
+
+static void matmul(const double* A, const double* B, double* C,
+                   int64_t M, int64_t K, int64_t N, int acc)
+{
+    if (acc == ACC_FP32)
         matmul_f32acc(A, B, C, M, K, N);
+    else if (acc == ACC_FP32_RZ16)
+        matmul_f32rz16(A, B, C, M, K, N);
     else
         matmul_f64(A, B, C, M, K, N);
 }
 
-/* C = A B (M x K times K x N, row-major fp64 arrays), accumulated in fp64
- * (acc32 == 0) or fp32 (acc32 != 0) as above. */
+/* C = A B (M x K times K x N, row-major fp64 arrays), accumulated as `acc`
+ * says: 0 fp64, 1 fp32 one rounding per addition, 2 fp32 round-toward-zero
+ * per 16-product block. */
 void oracle_matmul(const double* A, const double* B, double* C,
-                   int64_t M, int64_t K, int64_t N, int acc32)
+                   int64_t M, int64_t K, int64_t N, int acc)
 {
-    matmul(A, B, C, M, K, N, acc32);
+    matmul(A, B, C, M, K, N, acc);
 }
 
 static void transpose_f64(const double* X, double* XT, int64_t R, int64_t C)
@@ -189,12 +243,13 @@ static void transpose_f64(const double* X, double* XT, int64_t R, int64_t C)
  *   no steps the result is bf16( fl32(x_scale * X) ).
  * emulate_bf16 == 0: everything stays in fp64 (used to check the iteration
  *   against its singular-value closed form).
- * acc32 != 0 (with emulate_bf16 only): the three products are accumulated
- *   in fp32 (matmul_f32acc) instead of fp64; the spread variant. */
+ * acc != 0 (with emulate_bf16 only): the three products are accumulated
+ *   in fp32 (1: matmul_f32acc, 2: matmul_f32rz16) instead of fp64; the
+ *   spread variants. */
 int oracle_newton_schulz_ex(double* X, int64_t rows, int64_t cols, int steps,
-                            const float* coeffs, int emulate_bf16, float x_scale, int acc32)
+                            const float* coeffs, int emulate_bf16, float x_scale, int acc)
 {
-    if (acc32 && !emulate_bf16)
+    if (acc < 0 || acc > 2 || (acc && !emulate_bf16))
         return 1;
     if (rows <= 0 || cols <= 0 || steps < 0 || rows > cols || (steps > 0 && !coeffs))
         return 1;
@@ -217,7 +272,7 @@ int oracle_newton_schulz_ex(double* X, int64_t rows, int64_t cols, int steps,
         const float xs = s == 0 ? x_scale : 1.0f;  /* input scale, first step only */
         /* A = (xs X)(xs X)^T */
         transpose_f64(X, XT, rows, cols);
-        matmul(X, XT, A, rows, cols, rows, acc32);
+        matmul(X, XT, A, rows, cols, rows, acc);
         if (emulate_bf16) {
             const float xs2 = xs * xs;
             for (int64_t i = 0; i < rows * rows; ++i)
@@ -227,7 +282,7 @@ int oracle_newton_schulz_ex(double* X, int64_t rows, int64_t cols, int steps,
                 A[i] *= (double)xs * (double)xs;
         }
         /* B = b A + c A A */
-        matmul(A, A, AA, rows, rows, rows, acc32);
+        matmul(A, A, AA, rows, rows, rows, acc);
         for (int64_t i = 0; i < rows * rows; ++i) {
             if (emulate_bf16) {
                 float t1 = b * (float)A[i];
@@ -238,7 +293,7 @@ int oracle_newton_schulz_ex(double* X, int64_t rows, int64_t cols, int steps,
             }
         }
         /* X = a (xs X) + B (xs X) */
-        matmul(Bm, X, BX, rows, rows, cols, acc32);
+        matmul(Bm, X, BX, rows, rows, cols, acc);
         const float axs = a * xs;
         for (int64_t i = 0; i < rows * cols; ++i) {
             if (emulate_bf16) {
@@ -454,7 +509,9 @@ void oracle_step_stats(const float* u, const float* O, int64_t rows, int64_t col
  *   G   gradient, fp32 values (a bf16 gradient is passed already widened:
  *       the widening is exact)
  *   M   fp32 momentum, updated in place
- *   acc32             the NS products accumulate in fp32, not fp64
+ *   acc               how the NS products accumulate: 0 fp64, 1 fp32
+ *                     (one rounding per addition), 2 fp32 round-toward-
+ *                     zero per 16-product block
  *   cast_after_scale  X0 = bf16(u * s) and NS runs on it unscaled
  *                     (oracle_normalize_cast_after), instead of X0 =
  *                     bf16(u) with s applied inside the first NS step
@@ -467,7 +524,7 @@ int oracle_muon_step_matrix_ex(float* W, const float* G, float* M,
                                int64_t rows, int64_t cols,
                                const oracle_muon_hparams* hp,
                                float g_scale, int scale_g,
-                               int acc32, int cast_after_scale,
+                               int acc, int cast_after_scale,
                                float* X0_out, float* O_out)
 {
     if (rows <= 0 || cols <= 0 || !hp)
@@ -502,7 +559,7 @@ int oracle_muon_step_matrix_ex(float* W, const float* G, float* M,
         }
         coeffs = table;
     }
-    int rc = oracle_newton_schulz_ex(X, mp, np, hp->ns_steps, coeffs, 1, cast_after_scale ? 1.0f : s, acc32);
+    int rc = oracle_newton_schulz_ex(X, mp, np, hp->ns_steps, coeffs, 1, cast_after_scale ? 1.0f : s, acc);
     if (rc) {
         free(u); free(X); free(O);
         return 10 + rc;

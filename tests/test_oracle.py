@@ -458,9 +458,39 @@ def test_fp32_accumulation_is_ascending_and_rounds_every_sum():
     the pair pins both the precision and the order."""
     x = np.array([[1.0, 2.0 ** -12, 2.0 ** -12]])
     assert oracle.matmul(x, x.T)[0, 0] == 1.0 + 2.0 ** -23
-    assert oracle.matmul(x, x.T, acc32=True)[0, 0] == 1.0
+    assert oracle.matmul(x, x.T, accum=oracle.ACC_FP32)[0, 0] == 1.0
     r = x[:, ::-1].copy()
-    assert oracle.matmul(r, r.T, acc32=True)[0, 0] == 1.0 + 2.0 ** -23
+    assert oracle.matmul(r, r.T, accum=oracle.ACC_FP32)[0, 0] == 1.0 + 2.0 ** -23
+
+
+def test_blockwise_round_toward_zero_accumulation():
+    """ACC_FP32_RZ16: each run of 16 products is summed exactly and added
+    to the fp32 sum with one rounding toward zero.  Hand cases (all factors
+    bf16 values, so every product is exact):
+      * 1 in the first run and 3 * 2^-24 in the second: 1 + 1.5 ulp
+        truncates to 1 + 2^-23, where round-to-nearest (fp64 then fp32, or
+        fp32 throughout) ties to even at 1 + 2^-22;
+      * 1 and eight products of -2^-26 in one run: the run sums exactly to
+        1 - 2^-23, while one rounded-to-nearest fp32 addition per product
+        loses each -2^-26 (below half an ulp) and stays at 1."""
+    a = np.zeros((1, 32))
+    b = np.zeros((32, 1))
+    a[0, 0], b[0, 0] = 1.0, 1.0
+    a[0, 16], b[16, 0] = 3.0 * 2.0 ** -12, 2.0 ** -12
+    assert oracle.matmul(a, b, accum=oracle.ACC_FP32_RZ16)[0, 0] == 1.0 + 2.0 ** -23
+    assert oracle.matmul(a, b, accum=oracle.ACC_FP32)[0, 0] == 1.0 + 2.0 ** -22
+    assert np.float32(oracle.matmul(a, b)[0, 0]) == np.float32(1.0 + 2.0 ** -22)
+    a = np.array([[1.0] + [-2.0 ** -13] * 8])
+    b = np.array([[1.0] + [2.0 ** -13] * 8]).T
+    assert oracle.matmul(a, b, accum=oracle.ACC_FP32_RZ16)[0, 0] == 1.0 - 2.0 ** -23
+    assert oracle.matmul(a, b, accum=oracle.ACC_FP32)[0, 0] == 1.0
+    assert oracle.matmul(a, b)[0, 0] == 1.0 - 2.0 ** -23
+    # a negative sum truncates toward zero too: -(1 + 1.5 ulp) -> -(1 + 2^-23)
+    a = np.zeros((1, 17))
+    a[0, 0], a[0, 16] = -1.0, -3.0 * 2.0 ** -12
+    b = np.zeros((17, 1))
+    b[0, 0], b[16, 0] = 1.0, 2.0 ** -12
+    assert oracle.matmul(a, b, accum=oracle.ACC_FP32_RZ16)[0, 0] == -(1.0 + 2.0 ** -23)
 
 
 def test_fp32_accumulation_exact_on_small_integers():
@@ -472,7 +502,8 @@ def test_fp32_accumulation_exact_on_small_integers():
     B = rng.integers(-8, 9, size=(33, 5))
     ref = (A @ B).astype(np.float64)
     assert np.array_equal(oracle.matmul(A, B), ref)
-    assert np.array_equal(oracle.matmul(A, B, acc32=True), ref)
+    assert np.array_equal(oracle.matmul(A, B, accum=oracle.ACC_FP32), ref)
+    assert np.array_equal(oracle.matmul(A, B, accum=oracle.ACC_FP32_RZ16), ref)
 
 
 def test_ns_fp32_accumulation_exact_on_integer_input():
@@ -485,9 +516,9 @@ def test_ns_fp32_accumulation_exact_on_integer_input():
     A = X @ X.T
     ref = (X + (A + A @ A) @ X).astype(np.float64)
     assert np.abs(ref).max() < 256
-    for acc32 in (False, True):
-        got = oracle.newton_schulz(X.astype(np.float64), steps=1, coeffs=(1.0, 1.0, 1.0), acc32=acc32)
-        assert np.array_equal(got, ref), acc32
+    for accum in (oracle.ACC_FP64, oracle.ACC_FP32, oracle.ACC_FP32_RZ16):
+        got = oracle.newton_schulz(X.astype(np.float64), steps=1, coeffs=(1.0, 1.0, 1.0), accum=accum)
+        assert np.array_equal(got, ref), accum
 
 
 def test_ns_fp32_accumulation_stays_within_bf16_noise():
@@ -497,9 +528,10 @@ def test_ns_fp32_accumulation_stays_within_bf16_noise():
     from workloads import ns_input
     X = ns_input(96, 256, seed=4).float().numpy()
     a = oracle.newton_schulz(X)
-    b = oracle.newton_schulz(X, acc32=True)
-    rel = np.linalg.norm(a - b) / np.linalg.norm(a)
-    assert 0 < rel < 1e-2
+    for accum in (oracle.ACC_FP32, oracle.ACC_FP32_RZ16):
+        b = oracle.newton_schulz(X, accum=accum)
+        rel = np.linalg.norm(a - b) / np.linalg.norm(a)
+        assert 0 < rel < 1e-2, accum
 
 
 @pytest.mark.parametrize("shape", [(16, 64), (64, 16)])
@@ -541,8 +573,9 @@ def test_step_variants_route_through_the_staged_functions():
     hp = oracle.MuonConfig()
     _, u = oracle.momentum(G, M, hp.momentum, hp.nesterov)
     X0, s = oracle.normalize(u)
-    O32 = oracle.newton_schulz(X0, hp.ns_steps, x_scale=s, acc32=True).astype(np.float32)
-    assert np.array_equal(oracle.muon_step_matrix(W, G, M, hp, acc32=True)[3], O32)
+    for accum in (oracle.ACC_FP32, oracle.ACC_FP32_RZ16):
+        O32 = oracle.newton_schulz(X0, hp.ns_steps, x_scale=s, accum=accum).astype(np.float32)
+        assert np.array_equal(oracle.muon_step_matrix(W, G, M, hp, accum=accum)[3], O32)
     X0c, _ = oracle.normalize(u, cast_after_scale=True)
     Oc = oracle.newton_schulz(X0c, hp.ns_steps).astype(np.float32)
     assert np.array_equal(oracle.muon_step_matrix(W, G, M, hp, cast_after_scale=True)[3], Oc)
