@@ -5,6 +5,17 @@ the oracle.
 Per workload:
   * sampled matrices (seeded choice) run through the full oracle step:
     momentum M bit-exact, Muon update dW within rel. Frobenius 1e-2;
+  * the oracle's own spread beside the GPU's error: for one sampled matrix
+    of each distinct (m', n') the oracle also runs its variants, each as
+    faithful to the method as the reference evaluation -- the NS products
+    accumulated in fp32 with one rounding per addition (acc32) or with one
+    round-toward-zero per 16-product block (rz16, how tensor-core fp32
+    accumulation behaves in measurement), and the cast to bf16 after the
+    normalisation instead of before it (cast).  The GPU (fp32 accumulation
+    in the tensor cores, the reference's rounding points) must sit within
+    SPREAD_FACTOR of the larger fp32 spread, not merely under 1e-2.  With
+    MUON_PARITY_REPORT=<path> every comparison is appended there as one
+    JSON line;
   * every matrix (c2, c4): momentum M bit-exact against the oracle's
     element-wise momentum; every matrix (c1-c4): the update's
     singular-value content checked through the
@@ -14,6 +25,9 @@ Per workload:
     10 TFLOP per matrix on the CPU), so only the properties apply there,
     plus the band of the orthogonalised output's singular values.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -27,6 +41,11 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 TOL = 1e-2
 BUDGET = 16 << 30
+# The GPU's error against the fp64-accumulating oracle may be at most this
+# multiple of the larger of the acc32 and rz16 variants' errors: all three
+# accumulate in fp32, so they sit a similar distance from the fp64
+# evaluation (measured: the GPU at 0.96-1.10 times).
+SPREAD_FACTOR = 1.5
 
 
 def rel_fro(a, b):
@@ -52,14 +71,38 @@ def run_workload(name, sample):
     return w, t, host, W_before, hp
 
 
-def check_sampled(t, host):
+def report(rec):
+    path = os.environ.get("MUON_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+
+
+def check_sampled(t, host, w=None):
+    """Sampled matrices against the oracle; for the first sampled matrix of
+    each distinct (m', n') also the oracle's spread (acc32, rz16 and cast
+    variants)."""
     cfg = oracle_cfg()
+    seen = set()
     for i, (W0, G0, M0) in host.items():
         oW, oM, _, _ = oracle.muon_step_matrix(W0, G0, M0, cfg)
         assert np.array_equal(t.M[i].cpu().numpy(), oM), i
         W1 = t.W[i].cpu().numpy()
-        err = rel_fro(W1.astype(np.float64) - W0, oW.astype(np.float64) - W0)
+        W0d = W0.astype(np.float64)
+        d_ref = oW.astype(np.float64) - W0d
+        err = rel_fro(W1.astype(np.float64) - W0d, d_ref)
+        rec = {"workload": w.name if w else None, "matrix": i, "shape": list(W0.shape), "gpu_err": err}
+        key = (min(W0.shape), max(W0.shape))
+        if key not in seen:
+            seen.add(key)
+            for name, kw in (("acc32", dict(accum=oracle.ACC_FP32)), ("rz16", dict(accum=oracle.ACC_FP32_RZ16)),
+                             ("cast", dict(cast_after_scale=True))):
+                var = oracle.muon_step_matrix(W0, G0, M0, cfg, **kw)[0]
+                rec["spread_" + name] = rel_fro(var.astype(np.float64) - W0d, d_ref)
+        report(rec)
         assert err < TOL, (i, err)
+        if "spread_acc32" in rec:
+            assert err <= SPREAD_FACTOR * max(rec["spread_acc32"], rec["spread_rz16"]), rec
 
 
 def update_sigma_rms(W0, W1, hp, rows, cols):
@@ -92,7 +135,7 @@ def test_workload_fp32_grads(lib, name):
                 pick.append(i)
         sample = pick
     w, t, host, W_before, hp = run_workload(name, sample)
-    check_sampled(t, host)
+    check_sampled(t, host, w)
     check_update_rms(w, t, W_before, hp)
 
 
@@ -108,7 +151,7 @@ def test_workload_c2_dense_decoder(lib):
     M_all = [x.cpu().numpy() for x in t0.M]
     del t0
     w, t, host, W_before, hp = run_workload("c2", sample)
-    check_sampled(t, host)
+    check_sampled(t, host, w)
     for i in range(len(w.matrices)):
         oM, _ = oracle.momentum(G_all[i], M_all[i], hp.momentum, hp.nesterov)
         assert np.array_equal(t.M[i].cpu().numpy(), oM), i
@@ -167,9 +210,10 @@ def test_workload_c5_full_mixed_step(lib):
     """6144 expert matrices under Muon plus AdamW on the 163840x7168
     embedding and LM head, the largest workload."""
     w = workloads.get("c5")
-    sample = workloads.parity_sample(w)[:3]
+    sample = workloads.parity_sample(w)
+    sample = [sample[0], sample[-1]]   # a wide gate or up, and a tall down
     w, t, host, _, hp = run_workload("c5", sample)
-    check_sampled(t, host)
+    check_sampled(t, host, w)
     del t
     torch.cuda.empty_cache()
     ahp = m.AdamwHparams(**workloads.ADAMW_HPARAMS)

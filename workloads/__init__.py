@@ -235,6 +235,23 @@ def make_adamw(n: int, seed: int, device="cpu") -> AdamwTensors:
     return AdamwTensors(*out)
 
 
+def lowrank(rows: int, cols: int, seed: int, std: float, rank: int = 8, noise: float = 1e-3,
+            basis_seed: Optional[int] = None) -> torch.Tensor:
+    """An fp32 CPU matrix of rank `rank` plus i.i.d. noise, the shape real
+    gradients tend to take: L R with L (rows x rank) and R (rank x cols) of
+    i.i.d. normal draws, scaled to element standard deviation `std`, plus
+    noise * std * N(0, 1) per element.  `basis_seed` (default: `seed`)
+    draws L, so matrices that share it share their dominant column space."""
+    g_basis = torch.Generator().manual_seed(seed if basis_seed is None else basis_seed)
+    g = torch.Generator().manual_seed(seed + 7919)
+    r = min(rank, rows, cols)
+    left = torch.randn(rows, r, generator=g_basis, dtype=torch.float64)
+    right = torch.randn(r, cols, generator=g, dtype=torch.float64)
+    x = (left @ right) * (std / math.sqrt(r))
+    x += torch.randn(rows, cols, generator=g, dtype=torch.float64) * (noise * std)
+    return x.float()
+
+
 def ns_input(rows: int, cols: int, seed: int, kind: str = "gaussian") -> torch.Tensor:
     """A wide bf16 NS input of Frobenius norm close to 1 (CPU tensor).
 
