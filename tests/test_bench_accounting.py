@@ -33,3 +33,38 @@ def test_issued_never_below_algorithmic():
         alg = bench.ns_stage_flops(mp, np_)
         for k in alg:
             assert iss[k] >= alg[k], (mp, np_, k)
+
+
+def test_e2e_pieces_cover_every_element_once():
+    """The end-to-end run's pieces: runs of consecutive matrices whose
+    W, G, M fit a staging slot (one matrix per piece at least), then AdamW
+    chunks that tile each buffer exactly, every chunk starting 16-byte
+    aligned so the vector path stays on."""
+    from types import SimpleNamespace
+    import torch
+    import workloads
+
+    w = workloads.get("c3")
+    w.matrices = w.matrices[:40]                    # 4 attention + 36 expert matrices
+    n = sum(s.rows * s.cols for s in w.matrices)
+    storage = (torch.empty(n), torch.empty(n), torch.empty(n))
+    adamw = [SimpleNamespace(p=torch.empty(k), g=torch.empty(k), m=torch.empty(k), v=torch.empty(k))
+             for k in (1000, 37)]
+    ws = SimpleNamespace(w=w, tens=SimpleNamespace(storage=storage), adamw=adamw)
+    slot = 200 << 20
+    pieces = bench.e2e_pieces(ws, slot)
+    muon = [p for p in pieces if p[0] == "muon"]
+    ranges = [p[3] for p in muon]
+    assert ranges[0][0] == 0 and ranges[-1][1] == len(w.matrices)
+    assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
+    for kind, ins, outs, (a, b) in muon:
+        nbytes = sum(t.numel() * t.element_size() for t in ins)
+        assert b - a == 1 or nbytes <= slot
+        assert len(ins) == 3 and len(outs) == 2 and outs[0].data_ptr() == ins[0].data_ptr()
+    small = bench.e2e_pieces(ws, 64)                 # a slot smaller than any piece: one unit each
+    assert len([p for p in small if p[0] == "muon"]) == len(w.matrices)
+    for buf, want in zip(adamw, (1000, 37)):
+        chunks = [p[3] for p in small if p[0] == "adamw" and p[3][0].untyped_storage().data_ptr()
+                  == buf.p.untyped_storage().data_ptr()]
+        assert sum(q[0].numel() for q in chunks) == want
+        assert all(q[0].storage_offset() % 4 == 0 for q in chunks)
