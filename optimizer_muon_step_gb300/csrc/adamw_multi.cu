@@ -43,17 +43,18 @@ __global__ void __launch_bounds__(kThreads) adamw_multi_kernel(const __grid_cons
     for (int64_t j = first; j < nvec; j += stride) {
         while (j >= b.vec_begin[t + 1]) ++t;
         const int64_t i = 4 * (j - b.vec_begin[t]);
-        float4 pp = *reinterpret_cast<const float4*>(b.p[t] + i);
-        const float4 gg = __ldg(reinterpret_cast<const float4*>(b.g[t] + i));
-        float4 mm = *reinterpret_cast<const float4*>(b.m[t] + i);
-        float4 vv = *reinterpret_cast<const float4*>(b.v[t] + i);
+        // every byte is touched once: streaming (evict-first) loads and stores
+        float4 pp = __ldcs(reinterpret_cast<const float4*>(b.p[t] + i));
+        const float4 gg = __ldcs(reinterpret_cast<const float4*>(b.g[t] + i));
+        float4 mm = __ldcs(reinterpret_cast<const float4*>(b.m[t] + i));
+        float4 vv = __ldcs(reinterpret_cast<const float4*>(b.v[t] + i));
         adamw_elem(pp.x, gg.x, mm.x, vv.x, b.s);
         adamw_elem(pp.y, gg.y, mm.y, vv.y, b.s);
         adamw_elem(pp.z, gg.z, mm.z, vv.z, b.s);
         adamw_elem(pp.w, gg.w, mm.w, vv.w, b.s);
-        *reinterpret_cast<float4*>(b.p[t] + i) = pp;
-        *reinterpret_cast<float4*>(b.m[t] + i) = mm;
-        *reinterpret_cast<float4*>(b.v[t] + i) = vv;
+        __stcs(reinterpret_cast<float4*>(b.p[t] + i), pp);
+        __stcs(reinterpret_cast<float4*>(b.m[t] + i), mm);
+        __stcs(reinterpret_cast<float4*>(b.v[t] + i), vv);
     }
     const int64_t nsc = b.sc_begin[b.count];
     t = 0;
