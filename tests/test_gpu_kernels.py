@@ -79,7 +79,8 @@ def run_ns(shape, count, steps=5, coeffs=oracle.QUINTIC, seed=0, kind="gaussian"
 
 @pytest.mark.parametrize("coeffs,what", [((1.0, 0.0, 0.0), "identity"), ((0.0, 1.0, 0.0), "AX"),
                                          ((0.0, 0.0, 1.0), "AAX")])
-@pytest.mark.parametrize("shape", [(64, 64), (128, 256), (200, 328), (256, 512), (520, 1100), (512, 900)])
+@pytest.mark.parametrize("shape", [(64, 64), (128, 256), (200, 328), (256, 512), (520, 1100), (512, 900),
+                                   (1152, 1536)])
 def test_ns_single_stage_isolation(lib, shape, coeffs, what):
     """One step with one coefficient set isolates one product:
     (1,0,0) -> X;  (0,1,0) -> (X X^T) X;  (0,0,1) -> (X X^T)^2 X."""
@@ -102,10 +103,13 @@ def test_ns_single_stage_isolation(lib, shape, coeffs, what):
 # last pair row with 48 padded rows (between 1/16 and 1/8 of m', like the
 # 1408-row experts); (512, 832) and (768, 960) pair tiles on 64-aligned
 # shapes (chunked MN-major copies) with a ragged last column tile.
+# (1152, 1536), (1408, 2048) and (1408, 2112) run on pairs with a
+# half-empty last pair row (m' an odd multiple of 128), the last two with the
+# mixed step's expert rows and n' on and off the 256 grid.
 @pytest.mark.parametrize("shape", [(1, 1), (7, 13), (8, 8), (64, 64), (128, 256), (129, 257),
                                    (200, 328), (256, 512), (300, 1000), (384, 384), (464, 600), (520, 1100),
                                    (512, 512), (512, 832), (512, 900), (768, 800), (768, 960), (960, 1100),
-                                   (1000, 1100)])
+                                   (1000, 1100), (1152, 1536), (1408, 2048), (1408, 2112)])
 def test_ns_parity(lib, shape):
     count = 3 if shape[0] * shape[1] < 200_000 else 1
     X, got = run_ns(shape, count, seed=11)
@@ -158,7 +162,7 @@ def check_step(W0, G0, M0, W1, M1, hp):
 
 
 SHAPES = [(256, 512), (512, 256), (7, 13), (13, 7), (1, 1), (130, 70), (64, 1024), (300, 300),
-          (512, 900), (900, 512)]
+          (512, 900), (900, 512), (1152, 1536), (1536, 1152)]
 
 
 @pytest.mark.parametrize("gdt", [torch.float32, torch.bfloat16])
@@ -224,9 +228,10 @@ def test_step_zero_gradient_is_pure_decay(lib):
 def test_step_extreme_gradient_scale(lib, magnitude):
     """Norms far outside [2^-40, 2^40]: X0 is normalised in place before the
     first NS step instead of inside it (products of unnormalised bf16
-    elements would leave the normal fp32 range)."""
-    shapes = [(128, 256), (384, 128)]
-    W, G, M = make_mats(shapes, [torch.float32] * 2, seed=8)
+    elements would leave the normal fp32 range).  (1152, 1536) runs on CTA
+    pairs with a half-empty last pair row."""
+    shapes = [(128, 256), (384, 128), (1152, 1536)]
+    W, G, M = make_mats(shapes, [torch.float32] * len(shapes), seed=8)
     for g, mm in zip(G, M):
         g.mul_(magnitude / 1e-2)
         mm.mul_(magnitude / 1e-2)
@@ -242,9 +247,10 @@ def test_out_of_range_norm_path_is_exact(lib, p2):
     """Scaling G and M by a power of two scales u, bf16(u) and the norm
     exactly, so with norm_eps = 0 the NS input s * bf16(u) is unchanged.
     The scaled norms lie outside [2^-40, 2^40], where X0 takes a power of two
-    from the scale; the update must still be bit-identical."""
-    shapes = [(128, 256), (384, 128)]
-    W, G, M = make_mats(shapes, [torch.float32] * 2, seed=10)
+    from the scale; the update must still be bit-identical (also on the CTA
+    pairs of (1536, 1152), tall, with a half-empty last pair row)."""
+    shapes = [(128, 256), (384, 128), (1536, 1152)]
+    W, G, M = make_mats(shapes, [torch.float32] * len(shapes), seed=10)
     W2 = [w.clone() for w in W]
     G2 = [g * p2 for g in G]
     M2 = [x * p2 for x in M]
