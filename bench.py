@@ -738,11 +738,15 @@ class StagingRing:
         return out
 
 
+E2E_COPY_STREAMS = 2  # per direction: the host link carries more both ways with two (343 vs 312 GB/s)
+
+
 def run_e2e(m, ws: WorkloadStep, step_flops: int, world: int, barrier, max_over_ranks, n_steps: int,
             slot_bytes: int = E2E_SLOT_BYTES) -> dict:
-    """The step from host buffers and back through the public API, pipelined
-    over three streams: piece g+1's host->device copy, piece g's step and
-    piece g-1's device->host copy run concurrently."""
+    """The step from host buffers and back through the public API, pipelined:
+    piece g+1's host->device copy, piece g's step and piece g-1's
+    device->host copy run concurrently, the copies of successive pieces
+    alternating over E2E_COPY_STREAMS streams per direction."""
     import torch
     stream = torch.cuda.current_stream()
     pieces = e2e_pieces(ws, slot_bytes)
@@ -764,7 +768,8 @@ def run_e2e(m, ws: WorkloadStep, step_flops: int, world: int, barrier, max_over_
             ops.append(lambda st, batch=batch: batch.step(ws.hp, st))
         else:
             ops.append(lambda st, quad=what: m.adamw_step_batched([quad], ws.ahp, workloads.ADAMW_STEP, st))
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_ins = [torch.cuda.Stream() for _ in range(E2E_COPY_STREAMS)]
+    s_outs = [torch.cuda.Stream() for _ in range(E2E_COPY_STREAMS)]
     n = len(pieces)
     ev_in = [torch.cuda.Event() for _ in range(n)]
     ev_comp = [torch.cuda.Event() for _ in range(n)]
@@ -776,6 +781,7 @@ def run_e2e(m, ws: WorkloadStep, step_flops: int, world: int, barrier, max_over_
         for g, (kind, ins, outs, _) in enumerate(pieces):
             slot = counters[kind] % 2
             counters[kind] += 1
+            s_in, s_out = s_ins[g % E2E_COPY_STREAMS], s_outs[g % E2E_COPY_STREAMS]
             with torch.cuda.stream(s_in):
                 if ev_out[g] is not None:
                     s_in.wait_event(ev_out[g])
@@ -797,11 +803,14 @@ def run_e2e(m, ws: WorkloadStep, step_flops: int, world: int, barrier, max_over_
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
+    e0.record(stream)
+    for st in s_ins:
+        st.wait_event(e0)
     for _ in range(n_steps):
         one_step()
-    s_out.wait_stream(stream)
-    e1.record(s_out)
+    for st in s_outs:
+        stream.wait_stream(st)
+    e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / n_steps
     status = m.muon_query_status(ws.batch.workspace)
@@ -813,7 +822,7 @@ def run_e2e(m, ws: WorkloadStep, step_flops: int, world: int, barrier, max_over_
     return {"value": step_flops * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_steps,
             "pipeline": f"{n_muon} Muon pieces (runs of matrices) and {n - n_muon} AdamW chunks per step; "
-                        "copy in / step / copy out on 3 streams",
+                        f"copy in / step / copy out, {E2E_COPY_STREAMS} copy streams per direction",
             "host_buffers": f"pinned staging ring, 2 slots per kind and direction, "
                             f"{sum(r.bytes for r in rings.values()) / 2**30:.1f} GiB; input slots hold the "
                             "first (largest) piece's synthetic data, re-sent for every piece",
