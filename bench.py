@@ -915,16 +915,12 @@ def run_ours(args, rank, world, local_rank):
         line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": workload_config(w, ws_hp_steps(), world),
+                "config": workload_config(w, workloads.MUON_HPARAMS["ns_steps"], world),
                 "muon_ms_per_step": head["muon_ms_per_step"], "adamw": adamw,
                 "roofline": head["roofline"], "ns": head.get("ns"), "stages": head["stages"],
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": head["launches"], "clocks": head["clocks"],
                 "guarded_step": guard, "graph_replay": graph, "per_workload": per_workload}
         print(json.dumps(line), flush=True)
-
-
-def ws_hp_steps() -> int:
-    return int(workloads.MUON_HPARAMS["ns_steps"])
 
 
 def main():
