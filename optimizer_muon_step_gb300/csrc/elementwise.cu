@@ -108,6 +108,7 @@ template <int KIND>
 __global__ void __launch_bounds__(kThreads) momentum_norm_kernel(const MatDesc* __restrict__ descs,
                                                                  MomentumScalars s) {
     __shared__ float red[kThreads / 32];
+    pdl_wait_then_release();
     const MatDesc& d = descs[blockIdx.y];
     const int tile = blockIdx.x;
     // tall matrices: momentum_tall_kernel; other gradient types: their instance
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, KIND != MUON_F32 ? 4 : 6) momentum_t
     constexpr bool kPrefetch = KIND != MUON_F32;
     __shared__ uint16_t tileT[kTile][kTile + 2];
     __shared__ float red[kThreads / 32];
+    pdl_wait_then_release();
     const MatDesc& d = descs[blockIdx.y];
     const int unit = blockIdx.x;
     if (!d.transposed || unit >= d.nparts || d.g_kind != KIND) return;
@@ -336,6 +338,7 @@ constexpr double kNormHi = 1.099511627776e12;      // 2^40
 // One warp per matrix: fp64 sum of the partials in a fixed order.
 __global__ void __launch_bounds__(kThreads) norm_finalize_kernel(MatDesc* __restrict__ descs,
                                                                  int count, float eps, int force_rescale) {
+    pdl_wait_then_release();
     const int k = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (k >= count) return;
@@ -372,6 +375,7 @@ __global__ void __launch_bounds__(kThreads) norm_finalize_kernel(MatDesc* __rest
 constexpr int kRescaleCtas = 304;
 
 __global__ void __launch_bounds__(kThreads) x0_rescale_kernel(const MatDesc* __restrict__ descs, int count) {
+    pdl_wait_then_release();
     int flagged = 0;
     for (int k = threadIdx.x; k < count; k += kThreads) flagged |= descs[k].rescaled;
     if (!__syncthreads_or(flagged)) return;  // the usual case: nothing to do
@@ -406,6 +410,7 @@ __device__ __forceinline__ float update_elem(float w, float o, float sc, const U
 // 8 elements a thread per iteration.  grid = (max tiles, matrices).
 __global__ void __launch_bounds__(kThreads) final_update_wide_kernel(const MatDesc* __restrict__ descs,
                                                                      UpdateScalars us) {
+    pdl_wait_then_release();
     const MatDesc& d = descs[blockIdx.y];
     const int tile = blockIdx.x;
     if (d.transposed || tile >= d.ntiles) return;
@@ -457,6 +462,7 @@ inline __host__ __device__ int64_t final_tall_units(int64_t rows, int64_t cols) 
 __global__ void __launch_bounds__(kThreads, 4) final_update_tall_kernel(const MatDesc* __restrict__ descs,
                                                                         UpdateScalars us) {
     __shared__ uint16_t tileT[kTile][kTile + 2];
+    pdl_wait_then_release();
     const MatDesc& d = descs[blockIdx.y];
     const int unit = blockIdx.x;
     if (!d.transposed) return;
@@ -747,40 +753,49 @@ cudaError_t launch_desc_upload(MatDesc* d_descs, const MatDesc* descs, int count
 // muon_dtype_t; 0 when there are none of that type).
 cudaError_t launch_momentum_norm(const MatDesc* descs, int count, const int* wide_tiles, const int* tall_units,
                                  MomentumScalars s, cudaStream_t st) {
+    cudaError_t err = cudaSuccess;
+    auto keep = [&](cudaError_t e) { if (err == cudaSuccess) err = e; };
     for (int off = 0; off < count; off += 65535) {
         int n = count - off < 65535 ? count - off : 65535;
         if (wide_tiles[MUON_BF16] > 0) {
             launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-            momentum_norm_kernel<MUON_BF16><<<dim3(wide_tiles[MUON_BF16], n), kThreads, 0, st>>>(descs + off, s);
+            keep(launch_pdl(momentum_norm_kernel<MUON_BF16>, dim3(wide_tiles[MUON_BF16], n), dim3(kThreads), 0, st,
+                            descs + off, s));
             launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
         }
         if (wide_tiles[MUON_F16] > 0) {
             launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-            momentum_norm_kernel<MUON_F16><<<dim3(wide_tiles[MUON_F16], n), kThreads, 0, st>>>(descs + off, s);
+            keep(launch_pdl(momentum_norm_kernel<MUON_F16>, dim3(wide_tiles[MUON_F16], n), dim3(kThreads), 0, st,
+                            descs + off, s));
             launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
         }
         if (wide_tiles[MUON_F32] > 0) {
             launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-            momentum_norm_kernel<MUON_F32><<<dim3(wide_tiles[MUON_F32], n), kThreads, 0, st>>>(descs + off, s);
+            keep(launch_pdl(momentum_norm_kernel<MUON_F32>, dim3(wide_tiles[MUON_F32], n), dim3(kThreads), 0, st,
+                            descs + off, s));
             launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
         }
         if (tall_units[MUON_BF16] > 0) {
             launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-            momentum_tall_kernel<MUON_BF16><<<dim3(tall_units[MUON_BF16], n), kThreads, 0, st>>>(descs + off, s);
+            keep(launch_pdl(momentum_tall_kernel<MUON_BF16>, dim3(tall_units[MUON_BF16], n), dim3(kThreads), 0, st,
+                            descs + off, s));
             launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
         }
         if (tall_units[MUON_F16] > 0) {
             launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-            momentum_tall_kernel<MUON_F16><<<dim3(tall_units[MUON_F16], n), kThreads, 0, st>>>(descs + off, s);
+            keep(launch_pdl(momentum_tall_kernel<MUON_F16>, dim3(tall_units[MUON_F16], n), dim3(kThreads), 0, st,
+                            descs + off, s));
             launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
         }
         if (tall_units[MUON_F32] > 0) {
             launch_begin(MUON_KERNEL_MOMENTUM_NORM, st);
-            momentum_tall_kernel<MUON_F32><<<dim3(tall_units[MUON_F32], n), kThreads, 0, st>>>(descs + off, s);
+            keep(launch_pdl(momentum_tall_kernel<MUON_F32>, dim3(tall_units[MUON_F32], n), dim3(kThreads), 0, st,
+                            descs + off, s));
             launch_end(MUON_KERNEL_MOMENTUM_NORM, st);
         }
     }
-    return cudaGetLastError();
+    keep(cudaGetLastError());
+    return err;
 }
 
 int64_t final_update_tall_units(int64_t rows, int64_t cols) { return final_tall_units(rows, cols); }
@@ -788,32 +803,38 @@ int64_t final_update_tall_units(int64_t rows, int64_t cols) { return final_tall_
 cudaError_t launch_norm_finalize(MatDesc* descs, int count, float eps, int force_rescale, cudaStream_t st) {
     const int per = kThreads / 32;
     launch_begin(MUON_KERNEL_NORM_FINALIZE, st);
-    norm_finalize_kernel<<<(count + per - 1) / per, kThreads, 0, st>>>(descs, count, eps, force_rescale);
+    cudaError_t err = launch_pdl(norm_finalize_kernel, dim3((count + per - 1) / per), dim3(kThreads), 0, st, descs,
+                                 count, eps, force_rescale);
     launch_end(MUON_KERNEL_NORM_FINALIZE, st);
     launch_begin(MUON_KERNEL_X0_RESCALE, st);
-    x0_rescale_kernel<<<kRescaleCtas, kThreads, 0, st>>>(descs, count);
+    const cudaError_t e2 = launch_pdl(x0_rescale_kernel, dim3(kRescaleCtas), dim3(kThreads), 0, st, descs, count);
     launch_end(MUON_KERNEL_X0_RESCALE, st);
-    return cudaGetLastError();
+    if (err == cudaSuccess) err = e2;
+    if (err == cudaSuccess) err = cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_final_update(const MatDesc* descs, int count, int max_wide_tiles, int64_t max_tall_units,
                                 UpdateScalars s, cudaStream_t st) {
     if (max_tall_units > 0x7fffffff) return cudaErrorInvalidValue;
+    cudaError_t err = cudaSuccess;
+    auto keep = [&](cudaError_t e) { if (err == cudaSuccess) err = e; };
     for (int off = 0; off < count; off += 65535) {
         int n = count - off < 65535 ? count - off : 65535;
         if (max_wide_tiles > 0) {
             launch_begin(MUON_KERNEL_FINAL_UPDATE, st);
-            final_update_wide_kernel<<<dim3(max_wide_tiles, n), kThreads, 0, st>>>(descs + off, s);
+            keep(launch_pdl(final_update_wide_kernel, dim3(max_wide_tiles, n), dim3(kThreads), 0, st, descs + off, s));
             launch_end(MUON_KERNEL_FINAL_UPDATE, st);
         }
         if (max_tall_units > 0) {
             launch_begin(MUON_KERNEL_FINAL_UPDATE, st);
-            final_update_tall_kernel<<<dim3(static_cast<unsigned>(max_tall_units), n), kThreads, 0, st>>>(descs + off,
-                                                                                                       s);
+            keep(launch_pdl(final_update_tall_kernel, dim3(static_cast<unsigned>(max_tall_units), n), dim3(kThreads), 0,
+                            st, descs + off, s));
             launch_end(MUON_KERNEL_FINAL_UPDATE, st);
         }
     }
-    return cudaGetLastError();
+    keep(cudaGetLastError());
+    return err;
 }
 
 cudaError_t launch_grad_stats(const MatDesc* descs, int count, int max_tiles, WsHeader* header,

@@ -76,7 +76,39 @@ struct AdamwScalars {
     float bc1, bc2, eps, weight_decay;
 };
 
+// ---- programmatic dependent launch ------------------------------------------
+// The kernels of one step form a chain on one stream.  Those launched with
+// launch_pdl may be scheduled before the kernel ahead of them has finished:
+// each runs pdl_wait_then_release() before it touches global memory, which
+// waits until every kernel ahead of it has completed and its writes are
+// visible, and then lets the kernel behind it launch.  A chained kernel's
+// CTAs can thus start on idle SMs, and run any prologue that touches only
+// shared memory, TMEM and kernel parameters, while the kernel ahead
+// finishes.  Waiting before releasing keeps at most one kernel ahead.  After
+// a non-kernel stream operation (memset, copy, event) the launch falls back
+// to plain stream order.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 #ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // One AdamW element ("LLM training series, part 2: optimizers", sections 2.3
 // and 3.1), each operation a separately rounded fp32 op in this order:
 //   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g g

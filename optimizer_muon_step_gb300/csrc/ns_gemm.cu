@@ -593,6 +593,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) ns_gemm_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the prologue above touched only shared memory, TMEM and parameters
+    pdl_wait_then_release();
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
@@ -957,6 +959,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the prologue above touched only shared memory, TMEM and parameters
+    pdl_wait_then_release();
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer (both CTAs) ----------------
@@ -1309,16 +1313,18 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first
     constexpr int kind = MODE == MODE_SYRK ? MUON_KERNEL_NS_SYRK
                          : MODE == MODE_POLY ? MUON_KERNEL_NS_POLY : MUON_KERNEL_NS_UPDATE;
     launch_begin(kind, st);
+    cudaError_t e;
     if (kPair) {
         int pairs = max_pairs > 0 ? max_pairs : num_sms / 2;
         if (tiles < pairs) pairs = tiles;
-        ns_gemm_pair_kernel<MODE><<<2 * pairs, NUM_THREADS, PSMEM_BYTES, st>>>(prm);
+        e = launch_pdl(ns_gemm_pair_kernel<MODE>, dim3(2 * pairs), dim3(NUM_THREADS), PSMEM_BYTES, st, prm);
     } else {
         const int grid = tiles < num_sms ? tiles : num_sms;
-        ns_gemm_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(prm);
+        e = launch_pdl(ns_gemm_kernel<MODE>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, prm);
     }
     launch_end(kind, st);
-    return cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e;
 }
 
 // Whether a shape group runs on CTA pairs (all three stages).  Pairs halve
