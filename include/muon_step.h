@@ -151,10 +151,14 @@ muon_status_t muon_plan(const muon_matrix_t* mats, int64_t count,
  * be used by other work until the step has finished on `stream`.
  * count == 0 is a no-op.  A kernel that gives up on a bounded wait records
  * MUON_ERR_TIMEOUT in the workspace; read it with muon_query_status.
- * The call enqueues kernels and one memset only (no host<->device copy, no
- * synchronisation), so it may run inside a CUDA stream capture once one
- * call has run on the device outside a capture (the first call sets kernel
- * attributes); muon_step_graph_create needs no such call. */
+ * The call enqueues kernels only (no memset, no host<->device copy, no
+ * synchronisation; its first kernel clears the workspace status), so it may
+ * run inside a CUDA stream capture once one call has run on the device
+ * outside a capture (the first call sets kernel attributes);
+ * muon_step_graph_create needs no such call.  Its kernels are chained by
+ * programmatic dependent launch: each waits for the one ahead of it before
+ * it touches memory, so work the caller enqueues before or after the call
+ * on the same stream is ordered with it as usual. */
 muon_status_t muon_step_batched(const muon_matrix_t* mats, int64_t count,
                                 const muon_hparams_t* hp, void* workspace,
                                 size_t ws_bytes, void* stream);
@@ -221,8 +225,8 @@ muon_status_t muon_step_batched_noalloc(const muon_matrix_t* mats, int64_t count
 
 /* ---- The step as a CUDA graph (no counterpart on the pages) ------------- */
 
-/* muon_step_batched enqueues only kernels and one memset (the per-matrix
- * records travel as kernel parameters), so a caller may capture it into a
+/* muon_step_batched enqueues only kernels (the per-matrix records travel as
+ * kernel parameters), so a caller may capture it into a
  * CUDA graph of its own.  The calls below do that for the caller.
  *
  * A captured step replays the whole launch sequence of one

@@ -316,8 +316,7 @@ muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hpa
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     WsHeader* header = reinterpret_cast<WsHeader*>(ws);
-    s = from_cuda(cudaMemsetAsync(header, 0, sizeof(WsHeader), st));
-    if (s != MUON_OK) return s;
+    bool header_cleared = false;  // the call's first record upload clears the header
 
     const bool clip_on = hp->max_grad_norm > 0.f;
     const bool guard_on = clip_on || hp->skip_nonfinite;
@@ -405,7 +404,9 @@ muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hpa
                                                                 offsetof(MatDesc, ns_scale));
             L.groups[gi].scale_stride = static_cast<int64_t>(sizeof(MatDesc) / sizeof(float));
         }
-        return from_cuda(launch_desc_upload(d_descs, descs.data(), n, st));
+        WsHeader* clear = header_cleared ? nullptr : header;
+        header_cleared = true;
+        return from_cuda(launch_desc_upload(d_descs, descs.data(), n, clear, st));
     };
 
     // chunk boundaries

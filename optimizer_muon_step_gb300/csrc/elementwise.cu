@@ -705,6 +705,7 @@ inline unsigned grid_for(int64_t work, int64_t per_block, int64_t cap) {
 template <int K>
 struct DescBatch {
     MatDesc* dst;
+    WsHeader* zero_header;  // cleared by this launch before the records land; null: left alone
     int32_t count;
     MatDesc d[K];
 };
@@ -716,32 +717,43 @@ static_assert(sizeof(MatDesc) % 4 == 0, "word copy");
 template <int K>
 __global__ void __launch_bounds__(kThreads) desc_upload_kernel(const __grid_constant__ DescBatch<K> b) {
     constexpr int kWords = static_cast<int>(sizeof(MatDesc) / 4);
+    pdl_wait_then_release();
+    if (b.zero_header) {
+        uint32_t* h = reinterpret_cast<uint32_t*>(b.zero_header);
+        for (int i = threadIdx.x; i < static_cast<int>(sizeof(WsHeader) / 4); i += blockDim.x) h[i] = 0u;
+    }
     const uint32_t* src = reinterpret_cast<const uint32_t*>(b.d);
     uint32_t* dst = reinterpret_cast<uint32_t*>(b.dst);
     for (int i = threadIdx.x; i < b.count * kWords; i += blockDim.x) dst[i] = src[i];
 }
+static_assert(sizeof(WsHeader) % 4 == 0, "word clear");
 
 template <int K>
-cudaError_t upload_batch(MatDesc* d_descs, const MatDesc* descs, int count, cudaStream_t st) {
+cudaError_t upload_batch(MatDesc* d_descs, const MatDesc* descs, int count, WsHeader* zero_header,
+                         cudaStream_t st) {
     std::unique_ptr<DescBatch<K>> b(new (std::nothrow) DescBatch<K>());
     if (!b) return cudaErrorMemoryAllocation;
     b->dst = d_descs;
+    b->zero_header = zero_header;
     b->count = count;
     memcpy(b->d, descs, sizeof(MatDesc) * static_cast<size_t>(count));
     launch_begin(MUON_KERNEL_DESC_UPLOAD, st);
-    desc_upload_kernel<K><<<1, kThreads, 0, st>>>(*b);
+    cudaError_t e = launch_pdl(desc_upload_kernel<K>, dim3(1), dim3(kThreads), 0, st, *b);
     launch_end(MUON_KERNEL_DESC_UPLOAD, st);
-    return cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e;
 }
 
 }  // namespace
 
-cudaError_t launch_desc_upload(MatDesc* d_descs, const MatDesc* descs, int count, cudaStream_t st) {
+cudaError_t launch_desc_upload(MatDesc* d_descs, const MatDesc* descs, int count, WsHeader* zero_header,
+                               cudaStream_t st) {
     for (int done = 0; done < count;) {
         const int left = count - done;
         const int n = left < kUploadLarge ? left : kUploadLarge;
-        const cudaError_t e = n <= kUploadSmall ? upload_batch<kUploadSmall>(d_descs + done, descs + done, n, st)
-                                                : upload_batch<kUploadLarge>(d_descs + done, descs + done, n, st);
+        WsHeader* z = done == 0 ? zero_header : nullptr;
+        const cudaError_t e = n <= kUploadSmall ? upload_batch<kUploadSmall>(d_descs + done, descs + done, n, z, st)
+                                                : upload_batch<kUploadLarge>(d_descs + done, descs + done, n, z, st);
         if (e != cudaSuccess) return e;
         done += n;
     }

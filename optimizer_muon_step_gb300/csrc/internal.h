@@ -155,7 +155,11 @@ struct NvtxScope {
 // ---- per-matrix records (elementwise.cu) ----------------------------------
 // Writes descs[0..count) to d_descs on `st` through kernel parameters, so the
 // upload needs no host buffer that outlives the call (stream-capture safe).
-cudaError_t launch_desc_upload(MatDesc* d_descs, const MatDesc* descs, int count, cudaStream_t st);
+// With zero_header non-null the first upload kernel also clears that
+// workspace header (status word, guard results) before writing records: a
+// step starts with a clean header and no memset in its launch chain.
+cudaError_t launch_desc_upload(MatDesc* d_descs, const MatDesc* descs, int count, WsHeader* zero_header,
+                               cudaStream_t st);
 
 // ---- element-wise kernels (elementwise.cu) --------------------------------
 // Momentum pass: M updated, X0 = bf16(u) in the wide orientation (tall

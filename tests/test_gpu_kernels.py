@@ -316,3 +316,24 @@ def test_step_ragged_tall_multi_tile_units(lib, gdt):
     ws = m.muon_step_batched(W, G, M, hp)
     assert m.muon_query_status(ws) == 0
     check_step(*host[0], W[0].cpu().numpy(), M[0].cpu().numpy(), hp)
+
+
+def test_caller_kernel_after_the_step_sees_its_results(lib):
+    """The step's kernels are chained by programmatic dependent launch; a
+    kernel the caller enqueues next on the same stream (here torch's clone
+    and add, with no synchronisation in between) must still see the final W
+    and M.  Repeated over back-to-back steps, each checked against the
+    step computed once more on copies."""
+    shapes = [(256, 512), (512, 256), (1152, 1536)]
+    W, G, M = make_mats(shapes, [torch.float32] * len(shapes), seed=21)
+    Wr, Mr = [w.clone() for w in W], [x.clone() for x in M]
+    hp = m.MuonHparams()
+    ws = m.allocate_workspace(m.muon_workspace_size(shapes, 1 << 34))
+    for _ in range(3):
+        m.muon_step_batched(W, G, M, hp, workspace=ws)
+        seen_W = [w.clone() + 0.0 for w in W]     # caller kernels, same stream, no sync
+        seen_M = [x.clone() + 0.0 for x in M]
+        m.muon_step_batched(Wr, G, Mr, hp, workspace=ws)
+        torch.cuda.synchronize()
+        for a, b in zip(seen_W + seen_M, Wr + Mr):
+            assert torch.equal(a, b)
