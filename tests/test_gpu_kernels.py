@@ -337,3 +337,26 @@ def test_caller_kernel_after_the_step_sees_its_results(lib):
         torch.cuda.synchronize()
         for a, b in zip(seen_W + seen_M, Wr + Mr):
             assert torch.equal(a, b)
+
+
+def test_step_sees_a_gradient_the_caller_wrote_just_before(lib):
+    """The step's first kernel may launch before the caller's previous
+    kernel on the same stream has finished (programmatic dependent launch),
+    but it waits for it before reading: a gradient scaled by the caller's own
+    kernel right before the call, with no synchronisation, is the one the
+    step uses.  Checked against the step on a gradient scaled beforehand."""
+    shapes = [(256, 512), (1152, 1536)]
+    W, G, M = make_mats(shapes, [torch.float32] * len(shapes), seed=22)
+    W2, M2 = [w.clone() for w in W], [x.clone() for x in M]
+    G2 = [g * 3.0 for g in G]
+    torch.cuda.synchronize()
+    hp = m.MuonHparams()
+    ws = m.allocate_workspace(m.muon_workspace_size(shapes, 1 << 34))
+    m.muon_step_batched(W2, G2, M2, hp, workspace=ws)
+    torch.cuda.synchronize()
+    for g in G:
+        g.mul_(3.0)                               # the caller's kernel, same stream, no sync
+    m.muon_step_batched(W, G, M, hp, workspace=ws)
+    torch.cuda.synchronize()
+    for a, b in zip(W + M, W2 + M2):
+        assert torch.equal(a, b)
