@@ -80,7 +80,7 @@ def run_ns(shape, count, steps=5, coeffs=oracle.QUINTIC, seed=0, kind="gaussian"
 @pytest.mark.parametrize("coeffs,what", [((1.0, 0.0, 0.0), "identity"), ((0.0, 1.0, 0.0), "AX"),
                                          ((0.0, 0.0, 1.0), "AAX")])
 @pytest.mark.parametrize("shape", [(64, 64), (128, 256), (200, 328), (256, 512), (520, 1100), (512, 900),
-                                   (1152, 1536)])
+                                   (1152, 1536), (1370, 1500), (1600, 1664)])
 def test_ns_single_stage_isolation(lib, shape, coeffs, what):
     """One step with one coefficient set isolates one product:
     (1,0,0) -> X;  (0,1,0) -> (X X^T) X;  (0,0,1) -> (X X^T)^2 X."""
@@ -105,11 +105,15 @@ def test_ns_single_stage_isolation(lib, shape, coeffs, what):
 # shapes (chunked MN-major copies) with a ragged last column tile.
 # (1152, 1536), (1408, 2048) and (1408, 2112) run on pairs with a
 # half-empty last pair row (m' an odd multiple of 128), the last two with the
-# mixed step's expert rows and n' on and off the 256 grid.
+# mixed step's expert rows and n' on and off the 256 grid.  (1150, 1300) and
+# (1370, 1500) have ragged last pair rows of 126 and 90 rows on plain maps,
+# and (1600, 1664) one of 64 rows on chunked maps, where the second CTA's
+# half lies wholly past the matrix.
 @pytest.mark.parametrize("shape", [(1, 1), (7, 13), (8, 8), (64, 64), (128, 256), (129, 257),
                                    (200, 328), (256, 512), (300, 1000), (384, 384), (464, 600), (520, 1100),
                                    (512, 512), (512, 832), (512, 900), (768, 800), (768, 960), (960, 1100),
-                                   (1000, 1100), (1152, 1536), (1408, 2048), (1408, 2112)])
+                                   (1000, 1100), (1152, 1536), (1408, 2048), (1408, 2112), (1150, 1300),
+                                   (1370, 1500), (1600, 1664)])
 def test_ns_parity(lib, shape):
     count = 3 if shape[0] * shape[1] < 200_000 else 1
     X, got = run_ns(shape, count, seed=11)
