@@ -10,7 +10,12 @@
  * only enqueues work on the caller's CUDA stream and returns.  Pointers named
  * "device" must be CUDA device (or managed) memory of the current device;
  * pointers named "host" are ordinary host memory read before the call
- * returns.  No exception crosses this boundary; errors are returned as a
+ * returns.  Every call that launches kernels first asks the driver who owns
+ * each device buffer it is given (one query per allocation) and refuses host
+ * memory, another device's memory or an unknown address with
+ * MUON_ERR_INVALID_ARG before anything is enqueued; that check is left out
+ * while `stream` is being captured into a graph, where only launches are
+ * recorded.  No exception crosses this boundary; errors are returned as a
  * muon_status_t and describe host-side validation or launch failures, not
  * asynchronous kernel faults.  `stream` is a cudaStream_t passed as void*
  * (NULL = the legacy default stream).
@@ -29,7 +34,8 @@ extern "C" {
 
 typedef enum {
     MUON_OK = 0,
-    MUON_ERR_INVALID_ARG = 1,          /* null pointer, bad size, bad hparam  */
+    MUON_ERR_INVALID_ARG = 1,          /* null pointer, bad size, bad hparam,
+                                          a buffer not on the current device  */
     MUON_ERR_UNSUPPORTED_DTYPE = 2,    /* g_dtype not a muon_dtype_t          */
     MUON_ERR_MISALIGNED = 3,           /* pointer below its element alignment */
     MUON_ERR_WORKSPACE_TOO_SMALL = 4,  /* a single matrix needs more          */

@@ -11,9 +11,11 @@
 //   [n*8192, ...)            per shape group of c matrices:
 //                              X0[c], X1[c]  (each R(2 m' L(n')) bytes)
 //                              A[c],  B[c]   (each R(2 m' L(m')) bytes)
+#include <cuda.h>
 #include <math.h>
 
 #include <algorithm>
+#include <map>
 #include <memory>
 #include <mutex>
 #include <new>
@@ -55,6 +57,77 @@ muon_status_t device_info(int* num_sms) {
     if (d.ok != 1) return MUON_ERR_NO_DEVICE;
     *num_sms = d.num_sms;
     return MUON_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Whose memory the caller's buffers are.  Every buffer the kernels read or
+// write must be memory the current device owns: a device allocation made on
+// it, or managed memory.  Host memory (pinned or pageable), another device's
+// allocations and unknown addresses are refused with MUON_ERR_INVALID_ARG
+// before anything is enqueued, so such a call ends in an error code rather
+// than in a memory fault on the device.  Each driver query also looks up the
+// bounds of the allocation holding the pointer and remembers them, so the
+// views of one large buffer cost a single query.
+// ---------------------------------------------------------------------------
+typedef CUresult (*AddressRangeFn)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+AddressRangeFn address_range_fn() {
+    static AddressRangeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<AddressRangeFn>(ptr);
+    });
+    return fn;
+}
+
+class DeviceMemoryCheck {
+  public:
+    explicit DeviceMemoryCheck(int device) : dev_(device) {}
+
+    // Whether the buffer starting at p (bytes long) is the current device's.
+    bool owns(const void* p, size_t bytes) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        auto it = known_.upper_bound(lo);
+        if (it != known_.begin()) {
+            --it;
+            if (lo >= it->first && lo + bytes <= it->second) return true;
+        }
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+            cudaGetLastError();  // a refused query must not look like a failed launch later
+            return false;
+        }
+        const bool mine = (a.type == cudaMemoryTypeDevice && a.device == dev_) || a.type == cudaMemoryTypeManaged;
+        if (!mine) return false;
+        CUdeviceptr base = 0;
+        size_t size = 0;
+        const AddressRangeFn range = address_range_fn();
+        if (range && range(&base, &size, static_cast<CUdeviceptr>(lo)) == CUDA_SUCCESS && size > 0)
+            known_[static_cast<uintptr_t>(base)] = static_cast<uintptr_t>(base) + size;
+        return true;
+    }
+
+  private:
+    int dev_;
+    std::map<uintptr_t, uintptr_t> known_;  // verified allocations, start -> end
+};
+
+// Whether `st` is being captured into a graph.  A capture records launches
+// only, so the memory checks are left out there (muon_step_graph_create
+// checks before it captures); a stream whose state cannot be read counts as
+// capturing.
+bool capturing(cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return cs != cudaStreamCaptureStatusNone;
 }
 
 int64_t bytes_per_matrix(int64_t mp, int64_t np) {
@@ -128,6 +201,26 @@ muon_status_t check_pointers(const muon_matrix_t* mats, int64_t count) {
         if ((reinterpret_cast<uintptr_t>(m.W) & 3u) || (reinterpret_cast<uintptr_t>(m.M) & 3u) ||
             (reinterpret_cast<uintptr_t>(m.G) & (g_align - 1)))
             return MUON_ERR_MISALIGNED;
+    }
+    return MUON_OK;
+}
+
+// Every matrix's W, G and M, the workspace and the statistics array (when
+// given) on the current device.
+muon_status_t check_step_memory(const muon_matrix_t* mats, int64_t count, const void* workspace, size_t ws_bytes,
+                                const void* stats) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_NO_DEVICE;
+    DeviceMemoryCheck mem(dev);
+    if (!mem.owns(workspace, ws_bytes)) return MUON_ERR_INVALID_ARG;
+    if (stats && !mem.owns(stats, static_cast<size_t>(count) * sizeof(muon_matrix_stats_t)))
+        return MUON_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < count; ++i) {
+        const muon_matrix_t& m = mats[i];
+        const size_t n = static_cast<size_t>(m.rows * m.cols);
+        const size_t g_bytes = m.g_dtype == MUON_F32 ? 4 : 2;
+        if (!mem.owns(m.W, 4 * n) || !mem.owns(m.G, g_bytes * n) || !mem.owns(m.M, 4 * n))
+            return MUON_ERR_INVALID_ARG;
     }
     return MUON_OK;
 }
@@ -308,12 +401,16 @@ muon_status_t step_impl(const muon_matrix_t* mats, int64_t count, const muon_hpa
     int num_sms = 0;
     s = device_info(&num_sms);
     if (s != MUON_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!capturing(st)) {
+        s = check_step_memory(mats, count, workspace, ws_bytes, stats);
+        if (s != MUON_OK) return s;
+    }
 
     std::vector<PlanRow> plan;
     s = build_plan(mats, count, static_cast<int64_t>(ws_bytes), plan);
     if (s != MUON_OK) return s;
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     WsHeader* header = reinterpret_cast<WsHeader*>(ws);
     bool header_cleared = false;  // the call's first record upload clears the header
@@ -505,6 +602,8 @@ muon_status_t muon_step_graph_create(const muon_matrix_t* mats, int64_t count, c
         int num_sms = 0;
         s = device_info(&num_sms);
         if (s != MUON_OK) return s;
+        s = check_step_memory(mats, count, workspace, ws_bytes, nullptr);
+        if (s != MUON_OK) return s;
         // kernel attributes are set outside the capture
         if (ns_prepare_device() != cudaSuccess) return MUON_ERR_CUDA;
         cudaStream_t cs = nullptr;
@@ -570,6 +669,14 @@ muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t 
     muon_status_t s = device_info(&num_sms);
     if (s != MUON_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!capturing(st)) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_NO_DEVICE;
+        DeviceMemoryCheck mem(dev);
+        const size_t x_bytes = static_cast<size_t>(count * mp * np) * 2;
+        if (!mem.owns(X_in, x_bytes) || !mem.owns(X_out, x_bytes) || !mem.owns(workspace, ws_bytes))
+            return MUON_ERR_INVALID_ARG;
+    }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* status = reinterpret_cast<int*>(ws);
     s = from_cuda(cudaMemsetAsync(ws, 0, sizeof(WsHeader), st));
@@ -647,6 +754,22 @@ muon_status_t check_adamw_tensor(const float* p, const float* g, const float* m,
     return MUON_OK;
 }
 
+// One AdamW call's buffers on the current device (left out under capture).
+muon_status_t check_adamw_memory(const adamw_tensor_t* tensors, int64_t count, cudaStream_t st) {
+    if (capturing(st)) return MUON_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_NO_DEVICE;
+    DeviceMemoryCheck mem(dev);
+    for (int64_t i = 0; i < count; ++i) {
+        const adamw_tensor_t& x = tensors[i];
+        if (x.n == 0) continue;
+        const size_t bytes = static_cast<size_t>(x.n) * 4u;
+        if (!mem.owns(x.p, bytes) || !mem.owns(x.g, bytes) || !mem.owns(x.m, bytes) || !mem.owns(x.v, bytes))
+            return MUON_ERR_INVALID_ARG;
+    }
+    return MUON_OK;
+}
+
 // Whether byte ranges [start, end) are pairwise disjoint (sorted in place).
 bool disjoint(std::vector<std::pair<uintptr_t, uintptr_t>>& ranges) {
     std::sort(ranges.begin(), ranges.end());
@@ -679,6 +802,14 @@ muon_status_t adamw_step(float* p, const float* g, float* m, float* v, int64_t n
     int num_sms = 0;
     s = device_info(&num_sms);
     if (s != MUON_OK) return s;
+    adamw_tensor_t one;
+    one.p = p;
+    one.g = g;
+    one.m = m;
+    one.v = v;
+    one.n = n;
+    s = check_adamw_memory(&one, 1, static_cast<cudaStream_t>(stream));
+    if (s != MUON_OK) return s;
     return from_cuda(launch_adamw(p, g, m, v, n, sc, num_sms, static_cast<cudaStream_t>(stream)));
 }
 
@@ -706,6 +837,8 @@ muon_status_t adamw_step_batched(const adamw_tensor_t* tensors, int64_t count, c
     int num_sms = 0;
     s = device_info(&num_sms);
     if (s != MUON_OK) return s;
+    s = check_adamw_memory(tensors, count, static_cast<cudaStream_t>(stream));
+    if (s != MUON_OK) return s;
     return from_cuda(launch_adamw_multi(tensors, count, sc, num_sms, static_cast<cudaStream_t>(stream)));
 }
 
@@ -716,6 +849,12 @@ muon_status_t muon_check_bounded_wait(void* workspace, int64_t limit_us, void* s
     muon_status_t s = device_info(&num_sms);
     if (s != MUON_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!capturing(st)) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_NO_DEVICE;
+        DeviceMemoryCheck mem(dev);
+        if (!mem.owns(workspace, sizeof(WsHeader))) return MUON_ERR_INVALID_ARG;
+    }
     WsHeader* header = static_cast<WsHeader*>(workspace);
     s = from_cuda(cudaMemsetAsync(header, 0, sizeof(WsHeader), st));
     if (s != MUON_OK) return s;
