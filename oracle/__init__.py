@@ -25,7 +25,11 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "muon_oracle.c")
-_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+# MUON_ORACLE_LIB names a prebuilt variant of the library to load instead
+# (the test that plants mistakes in copies of muon_oracle.c uses it); it is
+# loaded as given and never rebuilt.
+_PREBUILT = os.environ.get("MUON_ORACLE_LIB")
+_LIB_PATH = _PREBUILT or os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -35,6 +39,8 @@ CFLAGS = ["-O3", "-std=c11", "-fPIC", "-shared", "-fopenmp",
 
 def build(force: bool = False) -> str:
     """Compile muon_oracle.c into liboracle.so (gcc, no GPU involved)."""
+    if _PREBUILT:
+        return _LIB_PATH
     stale = (not os.path.exists(_LIB_PATH)
              or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
     if force or stale:

@@ -239,6 +239,24 @@ def test_normalised_input_has_unit_norm():
     assert abs(np.linalg.norm(s * X0b.astype(np.float64)) - 1.0) < 2.0 ** -8
 
 
+def test_norm_eps_is_added_to_the_norm():
+    """The guard term sits outside the root, s = 1 / (||u|| + eps), as Adam
+    adds eps to sqrt(v) ([OPT] sections 2.2-2.3; the reading the step
+    takes).  With eps and the entries powers of two the normalised entries
+    are exact: a single entry eps gives eps / (eps + eps) = 1/2, a single
+    entry 3 eps gives 3/4, and the zero matrix gets s = 1/eps (its input stays
+    zero).  eps under the root would give about 2^-10 and 3 * 2^-10 here."""
+    eps = 2.0 ** -20
+    for entry, expect in ((eps, 0.5), (3 * eps, 0.75)):
+        u = np.zeros((4, 6), np.float32)
+        u[1, 2] = entry
+        X0, s = oracle.normalize(u, eps)
+        assert s * float(X0[1, 2]) == expect
+        assert np.count_nonzero(X0) == 1
+    X0, s = oracle.normalize(np.zeros((4, 6), np.float32), eps)
+    assert s == 2.0 ** 20 and not X0.any()
+
+
 def test_update_rms_matches_adamw_band():
     """[K2] section 3.1: the update is scaled to match AdamW's update RMS
     (0.2-0.4).  With wd = 0, dW = -lr * 0.2 sqrt(max(m,n)) O, and since
