@@ -68,6 +68,29 @@ MUTANTS = [
      "float g2 = gi * gi;", "float g2 = fabsf(gi);"),
     ("plan sort not stable on equal shapes",
      "if (om > cm || (om == cm && on > cn)) {", "if (om > cm || (om == cm && on >= cn)) {"),
+    ("fp32 accumulation in descending k",
+     "for (int64_t k = 0; k < K; ++k) {\n            const float a = (float)A[i * K + k];",
+     "for (int64_t k = K - 1; k >= 0; --k) {\n            const float a = (float)A[i * K + k];"),
+    ("block accumulation rounded to nearest instead of toward zero",
+     "c[j] = f32_toward_zero((double)c[j] + run[j]);", "c[j] = (float)((double)c[j] + run[j]);"),
+    ("first step's Gram matrix scaled by s instead of s^2",
+     "const float xs2 = xs * xs;", "const float xs2 = xs;"),
+    ("first step's update without s on B X",
+     "float t2 = xs * (float)BX[i];", "float t2 = (float)BX[i];"),
+    ("AdamW second moment corrected by the first moment's factor",
+     "float v_hat = vi / bc2;", "float v_hat = vi / bc1;"),
+    ("AdamW first moment decaying with beta2",
+     "float mi = hp->beta1 * m[i] + one_minus_b1 * gi;", "float mi = hp->beta2 * m[i] + one_minus_b1 * gi;"),
+    ("clip factor not capped at 1",
+     "return (float)(c < 1.0 ? c : 1.0);", "return (float)c;"),
+    ("guard counting NaN but not inf",
+     "if (!isfinite(G[k][i]))", "if (isnan(G[k][i]))"),
+    ("muP scale with the ratio inverted",
+     "double r = sqrt((double)rows / (double)cols);", "double r = sqrt((double)cols / (double)rows);"),
+    ("cast-after-scale reading rounding twice",
+     "const float scaled = u[r * cols + c] * s;", "const float scaled = bf16_round(u[r * cols + c]) * s;"),
+    ("update RMS averaged over one element too few",
+     "*update_rms = sqrt(so / (double)n);", "*update_rms = sqrt(so / (double)(n - 1));"),
 ]
 
 
