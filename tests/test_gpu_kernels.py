@@ -343,6 +343,50 @@ def test_caller_kernel_after_the_step_sees_its_results(lib):
             assert torch.equal(a, b)
 
 
+def test_step_over_more_matrices_than_one_launch_grid(lib):
+    """70,000 small matrices in one call and one workspace chunk: more than
+    the 65,535 rows one launch grid takes, so the momentum, final-update
+    and statistics passes each split into two launches, the records go up
+    in 313 uploads of up to 224, and one NS group holds them all.  Wide
+    8x16 and tall 16x8 matrices alternate, with fp32 and bf16 gradients.
+    Sampled matrices around the 65,535 boundary, the last one and a spread
+    between are checked against the oracle (momentum bit-exact, update
+    within the parity tolerance, statistics as in test_gpu_stats)."""
+    n = 70_000
+    shapes = [(8, 16) if i % 2 == 0 else (16, 8) for i in range(n)]
+    gen = torch.Generator(device=DEV).manual_seed(71)
+    Wf = torch.randn(n * 128, device=DEV, generator=gen) * 0.02
+    Gf = torch.randn(n * 128, device=DEV, generator=gen) * 1e-2
+    Gh = Gf.to(torch.bfloat16)
+    Mf = torch.randn(n * 128, device=DEV, generator=gen) * 1e-2
+    W = [Wf[128 * i:128 * (i + 1)].view(*shapes[i]) for i in range(n)]
+    G = [(Gh if i % 4 >= 2 else Gf)[128 * i:128 * (i + 1)].view(*shapes[i]) for i in range(n)]
+    M = [Mf[128 * i:128 * (i + 1)].view(*shapes[i]) for i in range(n)]
+    sample = sorted({0, 1, 2, 3, 65533, 65534, 65535, 65536, 65537, n - 2, n - 1} | set(range(97, n, 4999)))
+    W0 = {i: W[i].cpu().numpy() for i in sample}
+    G0 = {i: G[i].float().cpu().numpy() for i in sample}
+    M0 = {i: M[i].cpu().numpy() for i in sample}
+    hp = m.MuonHparams()
+    ws_bytes = m.muon_workspace_size(shapes, 1 << 34)
+    assert m.muon_plan(shapes, ws_bytes)["chunk_id"].max() == 0   # one chunk: every launch sees all 70,000
+    ws = m.allocate_workspace(ws_bytes)
+    stats = torch.empty(n, 2, dtype=torch.float64, device=DEV)
+    m.muon_step_batched(W, G, M, hp, workspace=ws, stats=stats)
+    torch.cuda.synchronize()
+    assert m.muon_query_status(ws) == 0
+    st = stats.cpu().numpy()
+    cfg = oracle.MuonConfig()
+    for i in sample:
+        oW, oM, _, O = oracle.muon_step_matrix(W0[i], G0[i], M0[i], cfg)
+        assert np.array_equal(M[i].cpu().numpy(), oM), i
+        dW = W[i].cpu().numpy().astype(np.float64) - W0[i]
+        assert rel_fro(dW, oW.astype(np.float64) - W0[i]) < NS_TOL, i
+        _, u = oracle.momentum(G0[i], M0[i], cfg.momentum, cfg.nesterov)
+        u_norm, rms = oracle.step_stats(u, O, cfg.rms_scale, cfg.scale_mode)
+        assert abs(st[i, 0] - u_norm) <= 1e-5 * u_norm, i
+        assert abs(st[i, 1] - rms) <= 2e-3 * rms, i
+
+
 def test_step_sees_a_gradient_the_caller_wrote_just_before(lib):
     """The step's first kernel may launch before the caller's previous
     kernel on the same stream has finished (programmatic dependent launch),
