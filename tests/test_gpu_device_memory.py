@@ -56,6 +56,8 @@ def test_muon_step_refuses_host_buffers(lib):
     assert call(W, [_pinned_like(G[0]), G[1]], M) == INVALID_ARG
     assert call(W, G, [M[0], _pinned_like(M[1])]) == INVALID_ARG
     assert call(W, G, M, workspace=_pinned_like(ws[:ws.numel()])) == INVALID_ARG
+    assert lib.muon_step_batched_noalloc(_muon_batch([W[0], _pinned_like(W[1])], G, M), 2, ctypes.byref(h),
+                                         stream) == INVALID_ARG
     stats = torch.empty(2 * 16, dtype=torch.uint8, pin_memory=True)
     assert lib.muon_step_batched_stats(_muon_batch(W, G, M), 2, ctypes.byref(h), ctypes.c_void_p(ws.data_ptr()),
                                        ws.numel(), ctypes.c_void_p(stats.data_ptr()), stream) == INVALID_ARG
