@@ -111,10 +111,11 @@ def ns_stage_issued_flops(mp: int, np_: int):
     diagonal tiles, rows and columns padded past the matrix and K rounded
     up to 64.  Mirrors the tile choices of the library's NS launch code:
     128x256 single-CTA tiles or 256x256 CTA-pair tiles (every stage on pairs
-    when 256-row pair tiles waste at most 1/8 of the rows),
+    when m' > 512 and 256-row pair tiles waste at most 1/8 of the rows),
     the last column tile rounded to 16 (single), 32 (pairs) or 128 (pairs on
     64-aligned shapes)."""
     pad = _ceil(mp, 256) * 256 - mp
+    pairs = mp > 512 and pad * 8 <= mp
     chunked = mp % 64 == 0 and np_ % 64 == 0
 
     def col_widths(n, pair):
@@ -126,7 +127,7 @@ def ns_stage_issued_flops(mp: int, np_: int):
         return out
 
     def triangle(k):
-        if pad * 8 <= mp:  # pairs: tiles (I, J >= I) of 256 x n_J
+        if pairs:  # pairs: tiles (I, J >= I) of 256 x n_J
             w = col_widths(mp, True)
             return sum(256 * w[j] * k for i in range(len(w)) for j in range(i, len(w)))
         w = col_widths(mp, False)
@@ -138,7 +139,7 @@ def ns_stage_issued_flops(mp: int, np_: int):
         return total
 
     k_x, k_g = _ceil(np_, 64) * 64, _ceil(mp, 64) * 64
-    if pad * 8 <= mp:
+    if pairs:
         upd = _ceil(mp, 256) * 256 * sum(col_widths(np_, True)) * k_g
     else:
         upd = _ceil(mp, 128) * 128 * sum(col_widths(np_, False)) * k_g

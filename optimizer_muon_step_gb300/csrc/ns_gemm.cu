@@ -1333,8 +1333,12 @@ cudaError_t launch_stage(const NsGroup* groups, int ngroups, int cur, bool first
 // a part-empty last pair row.  A group takes pairs when those are at most
 // 1/8 of its rows.  With two k-blocks per pair-ring stage this includes
 // the 1408-row MoE experts (9% padded rows) in every stage: their UPDATE
-// on pairs measured 1.7% faster than on single CTAs.
+// on pairs measured 1.7% faster than on single CTAs.  Up to 512 rows single
+// CTAs win (NS on 1200 matrices of 512 x 1024 14% faster, a lone 256 x 512
+// step 11% faster: no cluster launch or cross-CTA handshakes for one or two
+// row tiles); at 768 rows the two are level, at 1024 pairs lead by 6%.
 bool use_pairs(const NsGroup& g) {
+    if (g.mp <= 4 * BM) return false;
     const int64_t padded = (g.mp + 2 * BM - 1) / (2 * BM) * (2 * BM);
     return (padded - g.mp) * 8 <= g.mp;
 }

@@ -4,16 +4,26 @@ import bench
 
 
 def test_issued_equals_algorithmic_on_exact_pair_tiles_for_update():
-    # 512 x 1024: two 256-row pair rows, four 256-column tiles, K = 512
-    got = bench.ns_stage_issued_flops(512, 1024)
-    assert got["ns_update"] == 2 * 512 * 1024 * 512 == bench.ns_stage_flops(512, 1024)["ns_update"]
+    # 1024 x 2048: four 256-row pair rows, eight 256-column tiles, K = 1024
+    got = bench.ns_stage_issued_flops(1024, 2048)
+    assert got["ns_update"] == 2 * 1024 * 2048 * 1024 == bench.ns_stage_flops(1024, 2048)["ns_update"]
 
 
 def test_pair_triangle_counts_whole_diagonal_tiles():
-    # T = 2 pair rows -> tiles (0,0), (0,1), (1,1), each 256 x 256
+    # 1024 rows: 4 pair rows -> tiles (I, J >= I), 10 of 256 x 256
+    got = bench.ns_stage_issued_flops(1024, 2048)
+    assert got["ns_syrk"] == 2 * 10 * 256 * 256 * 2048
+    assert got["ns_poly"] == 2 * 10 * 256 * 256 * 1024
+
+
+def test_up_to_512_rows_run_on_single_ctas():
+    # 512 rows, no pair padding, but single CTAs: 4 row tiles of 128 over
+    # 2 column tiles of 256, odd diagonal tiles issuing only their right half:
+    # ti=0: 256 + 256; ti=1: 128 + 256; ti=2: 256; ti=3: 128
     got = bench.ns_stage_issued_flops(512, 1024)
-    assert got["ns_syrk"] == 2 * 3 * 256 * 256 * 1024
-    assert got["ns_poly"] == 2 * 3 * 256 * 256 * 512
+    assert got["ns_syrk"] == 2 * 128 * (512 + 384 + 256 + 128) * 1024
+    assert got["ns_poly"] == 2 * 128 * (512 + 384 + 256 + 128) * 512
+    assert got["ns_update"] == 2 * 512 * 1024 * 512
 
 
 def test_single_cta_triangle_skips_left_half_of_odd_diagonal_tiles():

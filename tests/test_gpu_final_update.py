@@ -14,7 +14,8 @@ W = 0 that:
   * W and M agree with the oracle (tolerances as in test_gpu_kernels.py).
 
 The shapes cover wide and tall matrices on both NS kernels (CTA pairs for
-256-row-aligned or lightly padded groups, single CTAs otherwise) with row
+256-row-aligned or lightly padded groups above 512 rows, single CTAs
+otherwise) with row
 and column counts that are not multiples of 32, 64, 128 or 256, after five
 NS steps and after none.
 """
@@ -74,8 +75,8 @@ def guard_mask(shapes):
 
 
 CASES = {
-    # CTA pairs: m' a multiple of 256, or at most 1/8 padding
-    "pairs": [(256, 520), (520, 256), (1024, 1090), (1090, 1024)],
+    # CTA pairs: m' above 512, a multiple of 256 or with at most 1/8 padding
+    "pairs": [(768, 1000), (1000, 768), (1024, 1090), (1090, 1024)],
     # single CTAs: m' with more than 1/8 pair padding; ragged everywhere
     "singles": [(130, 70), (70, 130), (300, 333), (333, 300), (33, 1000), (1000, 33)],
     "mixed": [(256, 512), (200, 328), (640, 1000), (1000, 640), (7, 13)],

@@ -93,16 +93,17 @@ def test_ns_single_stage_isolation(lib, shape, coeffs, what):
             assert rel_fro(got[i], ref) < NS_TOL, what
 
 
-# m' within 1/8 of a multiple of 256 runs on CTA pairs (256x256 pair
-# tiles, two 64-deep k-blocks per ring stage), other m' on single CTAs;
-# both kinds, ragged edges and odd k-block counts (a half-filled last
-# stage) included, are covered here.  Symmetric factors are read transposed
-# left of the diagonal block: (520, 1100) has single-CTA tiles whose two
-# 128-row halves of B take different layouts in one k-block, (1000, 1100)
-# and (960, 1100) pair tiles with a ragged last row block, (464, 600) a
-# last pair row with 48 padded rows (between 1/16 and 1/8 of m', like the
-# 1408-row experts); (512, 832) and (768, 960) pair tiles on 64-aligned
-# shapes (chunked MN-major copies) with a ragged last column tile.
+# m' above 512 and within 1/8 of a multiple of 256 runs on CTA pairs
+# (256x256 pair tiles, two 64-deep k-blocks per ring stage), other m' on
+# single CTAs; both kinds, ragged edges and odd k-block counts (a
+# half-filled last stage) included, are covered here.  Symmetric factors are
+# read transposed left of the diagonal block: (520, 1100) has single-CTA
+# tiles whose two 128-row halves of B take different layouts in one k-block,
+# (1000, 1100) and (960, 1100) pair tiles with a ragged last row block,
+# (720, 900) a last pair row with 48 padded rows (between 1/16 and 1/8 of m',
+# like the 1408-row experts); (768, 960) pair tiles on 64-aligned shapes
+# (chunked MN-major copies) with a ragged last column tile, and (512, 832)
+# the same shape class on single CTAs.
 # (1152, 1536), (1408, 2048) and (1408, 2112) run on pairs with a
 # half-empty last pair row (m' an odd multiple of 128), the last two with the
 # mixed step's expert rows and n' on and off the 256 grid.  (1150, 1300) and
@@ -110,7 +111,7 @@ def test_ns_single_stage_isolation(lib, shape, coeffs, what):
 # and (1600, 1664) one of 64 rows on chunked maps, where the second CTA's
 # half lies wholly past the matrix.
 @pytest.mark.parametrize("shape", [(1, 1), (7, 13), (8, 8), (64, 64), (128, 256), (129, 257),
-                                   (200, 328), (256, 512), (300, 1000), (384, 384), (464, 600), (520, 1100),
+                                   (200, 328), (256, 512), (300, 1000), (384, 384), (464, 600), (720, 900), (520, 1100),
                                    (512, 512), (512, 832), (512, 900), (768, 800), (768, 960), (960, 1100),
                                    (1000, 1100), (1152, 1536), (1408, 2048), (1408, 2112), (1150, 1300),
                                    (1370, 1500), (1600, 1664)])

@@ -54,7 +54,7 @@ def cfg_of(hp: m.MuonHparams) -> oracle.MuonConfig:
                              max_grad_norm=hp.max_grad_norm, ns_coeffs=hp.ns_coeffs)
 
 
-@pytest.mark.parametrize("shape", [(200, 328), (512, 900)])  # single-CTA and CTA-pair kernels
+@pytest.mark.parametrize("shape", [(200, 328), (768, 900)])  # single-CTA and CTA-pair kernels
 def test_ns_per_step_coefficients(lib, shape):
     X = torch.stack([workloads.ns_input(*shape, seed=21 + i) for i in range(2)]).to(DEV)
     got = m.muon_newton_schulz(X, steps=len(SCHEDULE), coeffs=SCHEDULE).float().cpu().numpy()
