@@ -700,20 +700,39 @@ muon_status_t muon_newton_schulz(const uint16_t* X_in, uint16_t* X_out, int64_t 
         g.X[1] = reinterpret_cast<uint16_t*>(cursor + cnt * g.x_stride);
         g.A = reinterpret_cast<uint16_t*>(cursor + 2 * cnt * g.x_stride);
         g.B = reinterpret_cast<uint16_t*>(cursor + 2 * cnt * g.x_stride + cnt * g.g_stride);
-        for (int64_t k = 0; k < cnt; ++k) {
-            s = from_cuda(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(g.X[0]) + k * g.x_stride, g.ldx * 2,
-                                            X_in + (first + k) * mp * np, row_bytes, row_bytes, mp,
+        // With rows a multiple of 8 wide the workspace rows are unpadded, so
+        // each matrix is one contiguous run and one strided copy moves the
+        // whole chunk (a matrix per copy "row", its pitch below the 2 GiB a
+        // copy pitch may reach); ragged widths copy matrix by matrix, row
+        // pitch and all.
+        const size_t mat_bytes = row_bytes * static_cast<size_t>(mp);
+        const bool whole = g.ldx == np && g.x_stride < (int64_t(1) << 31);
+        if (whole) {
+            s = from_cuda(cudaMemcpy2DAsync(g.X[0], g.x_stride, X_in + first * mp * np, mat_bytes, mat_bytes, cnt,
                                             cudaMemcpyDeviceToDevice, st));
             if (s != MUON_OK) return s;
+        } else {
+            for (int64_t k = 0; k < cnt; ++k) {
+                s = from_cuda(cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(g.X[0]) + k * g.x_stride, g.ldx * 2,
+                                                X_in + (first + k) * mp * np, row_bytes, row_bytes, mp,
+                                                cudaMemcpyDeviceToDevice, st));
+                if (s != MUON_OK) return s;
+            }
         }
         s = from_cuda(ns_run(&g, 1, ns_steps, coeffs.data(), status, num_sms, st));
         if (s != MUON_OK) return s;
         const uint16_t* res = g.X[ns_steps & 1];
-        for (int64_t k = 0; k < cnt; ++k) {
-            s = from_cuda(cudaMemcpy2DAsync(X_out + (first + k) * mp * np, row_bytes,
-                                            reinterpret_cast<const uint8_t*>(res) + k * g.x_stride, g.ldx * 2,
-                                            row_bytes, mp, cudaMemcpyDeviceToDevice, st));
+        if (whole) {
+            s = from_cuda(cudaMemcpy2DAsync(X_out + first * mp * np, mat_bytes, res, g.x_stride, mat_bytes, cnt,
+                                            cudaMemcpyDeviceToDevice, st));
             if (s != MUON_OK) return s;
+        } else {
+            for (int64_t k = 0; k < cnt; ++k) {
+                s = from_cuda(cudaMemcpy2DAsync(X_out + (first + k) * mp * np, row_bytes,
+                                                reinterpret_cast<const uint8_t*>(res) + k * g.x_stride, g.ldx * 2,
+                                                row_bytes, mp, cudaMemcpyDeviceToDevice, st));
+                if (s != MUON_OK) return s;
+            }
         }
     }
     return MUON_OK;

@@ -123,6 +123,22 @@ def test_ns_parity(lib, shape):
         assert rel_fro(got[i], ref) < NS_TOL, (shape, i)
 
 
+@pytest.mark.parametrize("shape", [(256, 512), (130, 300)])
+def test_ns_batches_in_several_passes_match_single_calls(lib, shape):
+    """Five matrices through a workspace that holds two run in three passes
+    (2, 2, 1); each result must equal the matrix run on its own, bit for
+    bit.  (256, 512) has unpadded workspace rows, so each pass moves its
+    matrices in and out with one strided copy; (130, 300) has padded rows
+    (300 is not a multiple of 8) and copies matrix by matrix."""
+    mp, np_ = shape
+    X = torch.stack([workloads.ns_input(mp, np_, 40 + i) for i in range(5)]).to(DEV)
+    ws = m.allocate_workspace(2 * m.muon_workspace_bytes_per_matrix(mp, np_))
+    got = m.muon_newton_schulz(X, workspace=ws)
+    for i in range(5):
+        alone = m.muon_newton_schulz(X[i:i + 1].contiguous())
+        assert torch.equal(got[i], alone[0]), i
+
+
 def test_ns_zero_steps_copies(lib):
     X, got = run_ns((40, 72), 2, steps=0)
     assert np.array_equal(X, got)
